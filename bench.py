@@ -1,0 +1,426 @@
+"""Benchmark of the owner-side Muon step on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference] [--no-e2e] [--no-cpu-baseline]
+
+Prints one JSON line.  `value` is the Muon step time (ms, lower is better) of
+the whole projection set with inputs resident in HBM; `e2e` is the same step
+through `dmuon_muon_step` with the gradients copied in from pinned host memory
+and the updated weights copied back inside the timed region.  The roofline
+entry covers the Newton-Schulz product kernel (tcgen05, bf16), which takes
+more than 90% of the step.  `--impl reference` times the fp64 CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "llama-3.1-8b"
+METRIC = "Muon step ms & NS TFLOP/s per model projection set (1 GB300); % bf16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 2 ** 20
+
+
+def _rank_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_record():
+    """DRAM bytes per launch of the product kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged (else None)."""
+    rec = os.path.join(ROOT, "profiles", "ns_gemm_traffic.json")
+    src = os.path.join(ROOT, "newton_schulz_owner_gb300", "csrc", "ns_gemm.cu")
+    if not os.path.exists(rec):
+        return None
+    with open(rec) as f:
+        d = json.load(f)
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()
+    if d.get("source_sha256") != h:
+        return None
+    return d
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(workload_name: str, budget_flops: float = 4.5e11):
+    """Time the fp64 oracle on a bounded sample of the workload and extrapolate
+    to one full Muon step (5 NS steps, every matrix).
+
+    The sample is one matrix of each of the cheapest distinct shapes, taken in
+    order of cost until about `budget_flops` nominal fp64 NS flops (1 step), run
+    through momentum, one Newton-Schulz step and the update.  The measured time
+    per NS flop and per element scales the sample to the whole set.
+    Returns (ms_per_full_step, description, seconds_spent)."""
+    import numpy as np
+    import oracle
+    from newton_schulz_owner_gb300 import workloads as wl
+
+    def nominal(s, k):   # dense fp64 flops of k NS steps: 4 m^2 n + 2 m^3 per step
+        m, n = min(s), max(s)
+        return k * (4.0 * m * m * n + 2.0 * m ** 3)
+
+    w = wl.WORKLOADS[workload_name]
+    shapes = w.shapes()
+    distinct = sorted(set(shapes), key=lambda s: nominal(s, 1))
+    sample, acc = [], 0.0
+    for s in distinct:
+        if sample and acc + nominal(s, 1) > budget_flops:
+            break
+        sample.append(s)
+        acc += nominal(s, 1)
+    rng = np.random.default_rng(0)
+    t_ns = t_ew = 0.0
+    f_ns = e_ew = 0.0
+    t_all = time.perf_counter()
+    for s in sample:
+        G = rng.standard_normal(s) * 1e-3
+        M = np.zeros(s)
+        W = rng.standard_normal(s) * 0.02
+        t0 = time.perf_counter()
+        M1, U = oracle.nesterov_momentum(G, M, 0.95)
+        t1 = time.perf_counter()
+        O = oracle.newton_schulz(U, 1)
+        t2 = time.perf_counter()
+        oracle.apply_update(W, O, 0.02)
+        t3 = time.perf_counter()
+        t_ew += (t1 - t0) + (t3 - t2)
+        e_ew += s[0] * s[1]
+        t_ns += t2 - t1
+        f_ns += nominal(s, 1)
+    spent = time.perf_counter() - t_all
+    total_s = sum(nominal(s, 5) for s in shapes) * (t_ns / f_ns) + \
+        sum(r * c for r, c in shapes) * (t_ew / e_ew)
+    desc = (f"fp64 oracle on one matrix of each of {len(sample)} of the {len(distinct)} "
+            f"distinct shapes of {workload_name} ({', '.join(f'{r}x{c}' for r, c in sample)}), "
+            f"1 NS step; scaled to all {len(shapes)} matrices x 5 NS steps by nominal "
+            f"flops (NS) and elements (momentum, update); extrapolated")
+    return total_s * 1e3, desc, spent
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    cores = os.cpu_count()
+    for _ in range(args.warmup):
+        oracle_sample(args.workload)
+    vals = []
+    for _ in range(args.steps):
+        ms, desc, _ = oracle_sample(args.workload)
+        vals.append(ms)
+    v = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "ms",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": v,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "ns_steps": 5,
+                                        "variant": "standard"},
+        "cpu_baseline": {"value": v, "unit": "ms", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": v, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+def count_launches(fn):
+    """Kernels launched by one call of fn(), counted with the CUDA profiler."""
+    import torch
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    n = 0
+    for ev in prof.events():
+        if ev.device_type is not None and "cuda" in str(ev.device_type).lower() and \
+                "dm::" in ev.name:
+            n += 1
+    return n
+
+
+def run_gpu(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from newton_schulz_owner_gb300 import build_lib
+    if not os.path.exists(build_lib.LIB):
+        build_lib.build()
+    from newton_schulz_owner_gb300 import dmuon
+    from newton_schulz_owner_gb300 import workloads as wl
+    import oracle
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+
+    w = wl.WORKLOADS[args.workload]
+    shapes = w.shapes()
+    n = len(shapes)
+    owner = dmuon.MuonOwner(shapes, n_owners=w.n_owners, variant=args.variant, device=dev)
+    G = wl.alloc_flat(shapes, w.grad_dtype, dev)
+    M = wl.alloc_flat(shapes, torch.float32, dev)
+    W = wl.alloc_flat(shapes, w.weight_dtype, dev)
+    wl.fill_grads(w, G, step=0)
+    wl.fill_weights(w, W)
+    stream = torch.cuda.Stream(device=dev)
+    ns_flops = (oracle.gram_ns_flops_algorithmic if args.variant == 1 else
+                oracle.ns_flops_algorithmic)(shapes, args.ns_steps)
+    if args.variant == 1:  # Gram only where n >= 2m; the rest run the standard form
+        gs = [s for s in shapes if max(s) >= 2 * min(s)]
+        ss = [s for s in shapes if max(s) < 2 * min(s)]
+        ns_flops = oracle.gram_ns_flops_algorithmic(gs, args.ns_steps) + \
+            oracle.ns_flops_algorithmic(ss, args.ns_steps)
+    elems = sum(r * c for r, c in shapes)
+
+    def step_phases(ev=None):
+        with torch.cuda.stream(stream):
+            if ev is not None:
+                ev[0].record(stream)
+            dmuon.pack(shapes, G.views, M.views, 0.95, owner.packed, owner.offsets,
+                       owner.workspace, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+            dmuon.ns_batched(shapes, owner.packed, owner.offsets, owner.workspace,
+                             ns_steps=args.ns_steps, variant=args.variant,
+                             use_pack_norms=True, stream=stream)
+            if ev is not None:
+                ev[2].record(stream)
+            dmuon.unpack_update(shapes, W.views, 0.02, owner.packed, owner.offsets,
+                                owner.workspace, stream=stream)
+            if ev is not None:
+                ev[3].record(stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step_phases()
+    barrier()
+    st = dmuon.stream_status(owner.workspace, stream)
+    if st != dmuon.OK:
+        raise RuntimeError(f"warm-up failed: {dmuon.status_string(st)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank if world > 1 else int(os.environ.get("GPU_INDEX", "0")))
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    for k in range(args.steps):
+        step_phases(evs[k])
+    barrier()
+    clocks = sampler.stop()
+    st = dmuon.stream_status(owner.workspace, stream)
+    if st != dmuon.OK:
+        raise RuntimeError(f"timed steps failed: {dmuon.status_string(st)}")
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    pack_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    ns_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    upd_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    t_total = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([t_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_total = float(t.item())
+    ms = t_total / args.steps
+    ns_mean = sum(ns_ms) / len(ns_ms)
+    achieved_tflops = ns_flops / (ns_mean * 1e-3) / 1e12
+
+    # ---- end to end through dmuon_muon_step with host buffers
+    e2e = None
+    if not args.no_e2e:
+        G_host = wl.alloc_flat(shapes, w.grad_dtype, "cpu", pin=True, zero=False)
+        W_host = wl.alloc_flat(shapes, w.weight_dtype, "cpu", pin=True, zero=False)
+        G_host.flat.copy_(G.flat)
+        h2d = G.flat.numel() * G.flat.element_size()
+        d2h = W.flat.numel() * W.flat.element_size()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                G.flat.copy_(G_host.flat, non_blocking=True)
+                owner.step(G.views, M.views, W.views, lr=0.02, beta=0.95,
+                           ns_steps=args.ns_steps, stream=stream)
+                W_host.flat.copy_(W.flat, non_blocking=True)
+
+        for _ in range(max(1, min(args.warmup, 2))):
+            e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        st = dmuon.stream_status(owner.workspace, stream)
+        if st != dmuon.OK:
+            raise RuntimeError(f"e2e steps failed: {dmuon.status_string(st)}")
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+        del G_host, W_host
+
+    launches_per_step = count_launches(lambda: step_phases())
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    tr = traffic_record()
+    roofline = {"bound": "tensor", "kernel": "ns_gemm_kernel (all Newton-Schulz products)",
+                "achieved": achieved_tflops, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved_tflops / peak, "peak_source": f"{peak_src} bf16 sustained",
+                "traffic": None if tr is None else tr.get("dram_bytes_per_launch"),
+                "flops_per_step": ns_flops}
+    elem_bytes = {"pack": (2 if w.grad_dtype == torch.bfloat16 else 4) + 4 + 4 + 2,
+                  "update": 2 + 2 * (2 if w.weight_dtype == torch.bfloat16 else 4)}
+    pack_mean = sum(pack_ms) / len(pack_ms)
+    upd_mean = sum(upd_ms) / len(upd_ms)
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    phases = {
+        "pack_ms": pack_mean, "ns_ms": ns_mean, "update_ms": upd_mean,
+        "pack_gbs": elems * elem_bytes["pack"] / (pack_mean * 1e-3) / 1e9,
+        "update_gbs": elems * elem_bytes["update"] / (upd_mean * 1e-3) / 1e9,
+        "hbm_peak_gbs": hbm_peak,
+    }
+    resident = (G.flat.numel() * G.flat.element_size() + M.flat.numel() * 4 +
+                W.flat.numel() * W.flat.element_size() + owner.packed.numel() * 2)
+    line = {
+        "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded normal gradients/weights shaped like the model's projections)",
+        "config": {"workload": args.workload, "matrices": n, "elements": elems,
+                   "ns_steps": args.ns_steps,
+                   "variant": "gram" if args.variant == 1 else "standard",
+                   "grad_dtype": str(w.grad_dtype).replace("torch.", ""),
+                   "weight_dtype": str(w.weight_dtype).replace("torch.", ""),
+                   "momentum_dtype": "float32", "parallelism": f"replicas x{world}",
+                   "l2": f"no flush: resident inputs {resident / 1e9:.1f} GB >> L2 "
+                         f"{L2_BYTES / 2**20:.0f} MB"},
+        "ns_tflops": achieved_tflops,
+        "matrices_per_s": n * world / (ms * 1e-3),
+        "phases": phases,
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        cms, desc, _ = oracle_sample(args.workload)
+        line["cpu_baseline"] = {"value": cms, "unit": "ms", "cores": os.cpu_count(),
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--ns-steps", type=int, default=5)
+    ap.add_argument("--variant", type=int, default=0, help="0 standard, 1 Gram")
+    ap.add_argument("--impl", default="dmuon", choices=["dmuon", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local_rank = _rank_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,191 @@
+/*
+ * dmuon.h -- C ABI of the DMuon owner-side Muon step on one GB300 (sm_103a).
+ *
+ * What the library computes (DMuon home page, "What DMuon Can Do" / "LLM
+ * Pretraining"; "Z2 vs Z3 Modes", "The two packed-buffer lifecycles"): the
+ * owner of a set of 2-D projection matrices runs, once per step,
+ *   1. Nesterov momentum on each gradient and packs the result (bf16) into one
+ *      contiguous per-owner buffer;
+ *   2. one Newton-Schulz orthogonalisation of every packed matrix
+ *      ("One owner. One Newton-Schulz.");
+ *   3. the scaled weight update.
+ * The pages name Muon and Newton-Schulz but do not write them out; the library
+ * uses the standard Muon forms:
+ *   M <- beta*M + (1-beta)*G,   U = (1-beta)*G + beta*M
+ *   X = U^T if rows > cols else U,   X0 = X / (||X||_F + eps)
+ *   ns_steps times: A = X X^T;  B = b*A + c*A*A;  X = a*X + B*X
+ *   O = X^T if transposed else X
+ *   W <- W - lr * sqrt(max(1, rows/cols)) * O
+ * with (a, b, c) = (3.4445, -4.7750, 2.0315) and eps = 1e-7 by default.
+ * The Gram variant (home page, "VLA and VLM": Gram Newton-Schulz) iterates on
+ * the m x m Gram matrix and gives the same result in exact arithmetic.
+ *
+ * Conventions shared by every call:
+ *  - A matrix is a PyTorch parameter of shape (rows, cols) = (out, in),
+ *    row-major and contiguous.  m = min(rows, cols), n = max(rows, cols).
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *    arrays that hold those pointers (grad[], momentum[], weight[]) and the
+ *    shape / offset arrays are HOST arrays, read during the call only.
+ *  - The library allocates no memory.  All scratch lives in the caller's
+ *    `workspace` (size from dmuon_workspace_bytes, 256-byte aligned); the
+ *    library copies its tables there with cudaMemcpyAsync on `stream`.
+ *  - Calls are asynchronous on `stream`.  Arguments are checked on the host
+ *    before anything is enqueued; a bad argument returns an error and
+ *    launches nothing.  Device-side failures (a bounded wait that gave up)
+ *    are recorded in the workspace and reported by dmuon_stream_status.
+ *  - Results are deterministic: the same inputs give bit-identical outputs
+ *    (no floating-point atomics; fixed reduction orders).
+ *  - NaN / Inf in the inputs propagate; nothing is clamped.  An all-zero
+ *    gradient gives O = 0, so W is unchanged.
+ *  - Calls that share a workspace must not overlap on the GPU.
+ */
+#ifndef DMUON_H
+#define DMUON_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every call. */
+typedef enum {
+  DMUON_OK = 0,
+  DMUON_ERR_INVALID_ARG = -1,  /* null pointer, bad size, bad enum, ns_steps < 0 ... */
+  DMUON_ERR_ALIGNMENT = -2,    /* packed / workspace not 256-byte aligned */
+  DMUON_ERR_WORKSPACE = -3,    /* ws_bytes < dmuon_workspace_bytes(...) */
+  DMUON_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed */
+  DMUON_ERR_TIMEOUT = -5,      /* a bounded device wait gave up (dmuon_stream_status) */
+  DMUON_ERR_UNSUPPORTED = -6   /* device is not sm_103 / shape beyond limits */
+} dmuon_status;
+
+/* Element types of caller tensors. */
+typedef enum { DMUON_F32 = 0, DMUON_BF16 = 1 } dmuon_dtype;
+
+/* Newton-Schulz variant. */
+typedef enum { DMUON_NS_STANDARD = 0, DMUON_NS_GRAM = 1 } dmuon_ns_variant;
+
+/* Shape of one parameter: PyTorch (out, in) = (rows, cols). */
+typedef struct { int64_t rows, cols; } dmuon_shape;
+
+/* Largest accepted m = min(rows, cols) and n = max(rows, cols). */
+#define DMUON_MAX_M 32768
+#define DMUON_MAX_N 1048576
+/* Element alignment of packed segments: 256 bytes of bf16. */
+#define DMUON_PACK_ALIGN_ELEMS 128
+
+/*
+ * dmuon_plan -- host-only owner assignment and packing offsets.
+ * Home page, "MoE": each matrix gets one owner and the partition is balanced
+ * so that no rank straggles; "Z2 vs Z3 Modes": the matrices of one owner share
+ * one contiguous buffer.  Reading: greedy LPT by element count (descending
+ * size, ties to the lower index; least-loaded owner, ties to the lower owner),
+ * then, owner by owner, segments in parameter order, each starting on a
+ * DMUON_PACK_ALIGN_ELEMS boundary, the owner buffers back to back in one
+ * allocation.
+ *   n            number of matrices (>= 1)
+ *   shp[n]       shapes (host)
+ *   n_owners     number of owner buffers (>= 1)
+ *   owner_of[n]  out: owner of each matrix (host)
+ *   offset[n]    out: element offset of each segment in the packed allocation
+ *   owner_elems[n_owners] out: elements of each owner buffer (padded)
+ * Returns DMUON_OK or DMUON_ERR_INVALID_ARG.  Touches no GPU.
+ */
+int dmuon_plan(int n, const dmuon_shape* shp, int n_owners, int* owner_of,
+               int64_t* offset, int64_t* owner_elems);
+
+/*
+ * dmuon_workspace_bytes -- scratch bytes that dmuon_pack / dmuon_ns_batched /
+ * dmuon_unpack_update / dmuon_muon_step need for this shape list and variant.
+ * Returns 0 for invalid arguments.  Touches no GPU.
+ */
+size_t dmuon_workspace_bytes(int n, const dmuon_shape* shp, int ns_variant);
+
+/*
+ * dmuon_pack -- Nesterov momentum + pack (step 1 above).
+ * For each matrix i: M_i <- beta*M_i + (1-beta)*G_i (fp32, in place) and
+ * packed[offset[i] + k] = bf16_rne(U_i[k]) with U_i = (1-beta)*G_i + beta*M_i,
+ * in the parameter's own (rows, cols) row-major order.  Also records
+ * ||U_i||_F^2 partial sums (fp32, fixed order) in the workspace; a following
+ * dmuon_ns_batched(..., use_pack_norms=1) uses them as the norm of the fp32 U.
+ *   grad[n]      device pointers, dtype grad_dt (F32 or BF16)
+ *   momentum[n]  device pointers, fp32, updated in place
+ *   packed_bf16  device, 256-byte aligned, >= max(offset[i] + rows*cols) bf16
+ *   offset[n]    element offsets (multiples of DMUON_PACK_ALIGN_ELEMS)
+ */
+int dmuon_pack(int n, const dmuon_shape* shp, const void* const* grad, int grad_dt,
+               float* const* momentum, float beta, void* packed_bf16,
+               const int64_t* offset, void* workspace, size_t ws_bytes,
+               cudaStream_t stream);
+
+/*
+ * dmuon_ns_batched -- Newton-Schulz orthogonalisation of every packed matrix,
+ * in place (step 2 above).  packed[offset[i] ...] holds U_i (bf16, (rows, cols)
+ * row-major) on entry and O_i (bf16, same layout) on return.
+ *   ns_steps       >= 0; 0 returns X0 = U / (||U||_F + eps)
+ *   ns_variant     DMUON_NS_STANDARD or DMUON_NS_GRAM
+ *   abc            host float[3] (a, b, c), or NULL for (3.4445, -4.7750, 2.0315)
+ *   eps            norm epsilon (the standard value is 1e-7)
+ *   use_pack_norms 1: take ||U_i|| from the partial sums of the preceding
+ *                  dmuon_pack on this workspace (fp32 U); 0: compute it from
+ *                  the bf16 values in `packed`.
+ * Products run on the tcgen05 tensor cores with bf16 operands and fp32
+ * accumulation; A and B are stored bf16.
+ */
+int dmuon_ns_batched(int n, const dmuon_shape* shp, void* packed_bf16,
+                     const int64_t* offset, int ns_steps, int ns_variant,
+                     const float* abc, float eps, int use_pack_norms,
+                     void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * dmuon_unpack_update -- scaled weight update (step 3 above):
+ * W_i <- W_i - lr * sqrt(max(1, rows/cols)) * O_i, O_i read from packed.
+ * fp32 arithmetic; a bf16 W is rounded to nearest even.
+ *   weight[n]   device pointers, dtype weight_dt (F32 or BF16), in place
+ */
+int dmuon_unpack_update(int n, const dmuon_shape* shp, void* const* weight,
+                        int weight_dt, float lr, const void* packed_bf16,
+                        const int64_t* offset, void* workspace, size_t ws_bytes,
+                        cudaStream_t stream);
+
+/*
+ * dmuon_muon_step -- the whole owner-side Muon step: dmuon_pack, then
+ * dmuon_ns_batched(use_pack_norms = 1) with the default coefficients and
+ * eps = 1e-7, then dmuon_unpack_update, enqueued on `stream`.
+ */
+int dmuon_muon_step(int n, const dmuon_shape* shp, const void* const* grad, int grad_dt,
+                    float* const* momentum, void* const* weight, int weight_dt,
+                    float lr, float beta, int ns_steps, int ns_variant,
+                    void* packed_bf16, const int64_t* offset, void* workspace,
+                    size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * dmuon_stream_status -- synchronises `stream`, then reports (and clears) the
+ * device error word kept in `workspace`: DMUON_OK, DMUON_ERR_TIMEOUT when a
+ * bounded device wait gave up, DMUON_ERR_CUDA when the stream holds a CUDA
+ * error.  workspace may be NULL (then only the stream is checked).
+ */
+int dmuon_stream_status(cudaStream_t stream, void* workspace);
+
+/*
+ * dmuon_debug_wait_timeout -- test hook for the device failure path: launches
+ * one block that waits on a shared-memory barrier nobody signals, with a
+ * limit of `budget_us` microseconds (1..1000000).  The wait gives up, the
+ * kernel records DMUON_ERR_TIMEOUT in the workspace error word and returns,
+ * leaving the context usable.  Needs ws_bytes >= 256.
+ */
+int dmuon_debug_wait_timeout(void* workspace, size_t ws_bytes, int budget_us,
+                             cudaStream_t stream);
+
+/* Human-readable text for a status code (static storage). */
+const char* dmuon_status_string(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int dmuon_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DMUON_H */

@@ -1,0 +1,673 @@
+// C ABI of the owner-side Muon step: argument checks, planning, workspace
+// layout, tensor maps, and the launch sequence.  See include/dmuon.h.
+#include "dmuon.h"
+#include "launch.h"
+#include "tables.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+namespace dm {
+namespace {
+
+constexpr size_t kHdrBytes = 256;  // workspace header: device error word
+constexpr int kMaxNsSteps = 1000;
+constexpr int kMaxDevices = 64;
+constexpr float kDefaultAbc[3] = {3.4445f, -4.7750f, 2.0315f};
+constexpr float kDefaultEps = 1e-7f;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------------ planning
+struct BucketPlan {
+  int m = 0, n = 0;
+  bool gram = false;
+  std::vector<int> mats;  // caller indices, in caller order
+  int pitch_x = 0, pitch_m = 0;
+  long long stride_x = 0, stride_m = 0;
+  bool used[kSlots] = {};
+  size_t slot_off[kSlots] = {};
+  std::vector<int> sym;   // (ti << 16) | tj, upper-triangle tiles of an m x m product
+  int full_ti = 0, full_tj = 0;
+};
+
+struct Plan {
+  int n = 0;
+  std::vector<BucketPlan> buckets;  // standard buckets first, then Gram buckets
+  int n_std = 0;                    // number of standard buckets
+  std::vector<int> bucket_of, idx_in_bucket, internal_of;
+  std::vector<long long> chunk_begin, tile_begin;
+  std::vector<int> n_chunks, tiles_r, tiles_c;
+  long long total_chunks = 0, total_tiles = 0;
+  int n_internal = 0;
+  int sym_total = 0;
+  size_t off_tables = 0, tables_bytes = 0;
+  size_t off_ew = 0, off_bk = 0, off_imat = 0, off_sym = 0, off_tmaps = 0;
+  size_t off_partials = 0, off_inv = 0;
+  size_t total = 0;
+};
+
+bool shape_ok(const dmuon_shape& s) {
+  if (s.rows < 0 || s.cols < 0) return false;
+  if (s.rows == 0 || s.cols == 0) return true;
+  const int64_t m = std::min(s.rows, s.cols), n = std::max(s.rows, s.cols);
+  return m <= DMUON_MAX_M && n <= DMUON_MAX_N;
+}
+
+bool uses_gram(int variant, int m, int n) {
+  // Reading: the Gram form only for clearly rectangular matrices (n >= 2m),
+  // where it also saves work; square-ish matrices keep the standard form.
+  return variant == DMUON_NS_GRAM && n >= 2 * m;
+}
+
+int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
+  if (n < 0 || (n > 0 && shp == nullptr)) return DMUON_ERR_INVALID_ARG;
+  if (variant != DMUON_NS_STANDARD && variant != DMUON_NS_GRAM) return DMUON_ERR_INVALID_ARG;
+  P = Plan();
+  P.n = n;
+  P.bucket_of.assign(n, -1);
+  P.idx_in_bucket.assign(n, -1);
+  P.internal_of.assign(n, -1);
+  P.chunk_begin.assign(n, 0);
+  P.tile_begin.assign(n, 0);
+  P.n_chunks.assign(n, 0);
+  P.tiles_r.assign(n, 0);
+  P.tiles_c.assign(n, 0);
+
+  // buckets keyed by (gram, m, n); standard first, each group in first-seen order
+  std::map<std::tuple<int, int, int>, int> key_to_b;
+  std::vector<std::tuple<int, int, int>> order;
+  for (int i = 0; i < n; ++i) {
+    if (!shape_ok(shp[i])) return DMUON_ERR_INVALID_ARG;
+    const long long r = shp[i].rows, c = shp[i].cols;
+    P.n_chunks[i] = int(ceil_div(r * c, kChunk));
+    P.tiles_r[i] = int(ceil_div(r, kRelayTile));
+    P.tiles_c[i] = int(ceil_div(c, kRelayTile));
+    P.chunk_begin[i] = P.total_chunks;
+    P.tile_begin[i] = P.total_tiles;
+    P.total_chunks += P.n_chunks[i];
+    P.total_tiles += (long long)P.tiles_r[i] * P.tiles_c[i];
+    if (r == 0 || c == 0) continue;
+    const int m = int(std::min(r, c)), nn = int(std::max(r, c));
+    const auto key = std::make_tuple(uses_gram(variant, m, nn) ? 1 : 0, m, nn);
+    if (!key_to_b.count(key)) {
+      key_to_b[key] = -1;
+      order.push_back(key);
+    }
+  }
+  std::stable_sort(order.begin(), order.end(),
+                   [](const auto& a, const auto& b) { return std::get<0>(a) < std::get<0>(b); });
+  for (size_t b = 0; b < order.size(); ++b) {
+    key_to_b[order[b]] = int(b);
+    BucketPlan bp;
+    bp.gram = std::get<0>(order[b]) != 0;
+    bp.m = std::get<1>(order[b]);
+    bp.n = std::get<2>(order[b]);
+    P.buckets.push_back(bp);
+    if (!bp.gram) P.n_std = int(b) + 1;
+  }
+  for (int i = 0; i < n; ++i) {
+    const long long r = shp[i].rows, c = shp[i].cols;
+    if (r == 0 || c == 0) continue;
+    const int m = int(std::min(r, c)), nn = int(std::max(r, c));
+    const int b = key_to_b[std::make_tuple(uses_gram(variant, m, nn) ? 1 : 0, m, nn)];
+    P.bucket_of[i] = b;
+    P.idx_in_bucket[i] = int(P.buckets[b].mats.size());
+    P.buckets[b].mats.push_back(i);
+  }
+  int internal = 0;
+  for (auto& B : P.buckets) {
+    for (int i : B.mats) P.internal_of[i] = internal++;
+    B.pitch_x = int(align_up(size_t(B.n), 64));
+    B.pitch_m = int(align_up(size_t(B.m), 64));
+    B.stride_x = (long long)B.m * B.pitch_x;
+    B.stride_m = (long long)B.m * B.pitch_m;
+    if (!B.gram) {
+      B.used[SX0] = B.used[SX1] = B.used[SM0] = B.used[SM1] = true;
+    } else {
+      B.used[SX0] = true;
+      for (int s = SM0; s <= SM5; ++s) B.used[s] = true;
+    }
+    const int I = int(ceil_div(B.m, kBM)), J = int(ceil_div(B.m, kBN));
+    for (int ti = 0; ti < I; ++ti)
+      for (int tj = (ti * kBM) / kBN; tj < J; ++tj) B.sym.push_back((ti << 16) | tj);
+    B.full_ti = I;
+    B.full_tj = int(ceil_div(B.n, kBN));
+    P.sym_total += int(B.sym.size());
+  }
+  P.n_internal = internal;
+
+  // workspace layout
+  size_t off = kHdrBytes;
+  P.off_tables = off;
+  P.off_ew = off;
+  off = align_up(off + size_t(n) * sizeof(EwMat), 16);
+  P.off_bk = off;
+  off = align_up(off + P.buckets.size() * sizeof(Bucket), 16);
+  P.off_imat = off;
+  off = align_up(off + size_t(P.n_internal) * sizeof(InternalMat), 16);
+  P.off_sym = off;
+  off = align_up(off + size_t(P.sym_total) * sizeof(int), 128);
+  P.off_tmaps = off;
+  off = align_up(off + P.buckets.size() * kSlots * 128, 16);
+  P.tables_bytes = off - P.off_tables;
+  off = align_up(off, 256);
+  P.off_partials = off;
+  off = align_up(off + size_t(P.total_chunks) * sizeof(float), 256);
+  P.off_inv = off;
+  off = align_up(off + size_t(n) * sizeof(float), 4096);
+  for (auto& B : P.buckets) {
+    for (int s = 0; s < kSlots; ++s) {
+      if (!B.used[s]) continue;
+      B.slot_off[s] = off;
+      const long long stride = slot_is_x(s) ? B.stride_x : B.stride_m;
+      off = align_up(off + size_t(B.mats.size()) * size_t(stride) * 2, 4096);
+    }
+  }
+  P.total = off;
+  return DMUON_OK;
+}
+
+// ------------------------------------------------------------------ device
+struct DevInfo {
+  bool ready = false;
+  int status = DMUON_OK;
+  int sms = 0;
+  int clock_khz = 0;
+};
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+
+int device_info(DevInfo* out) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return DMUON_ERR_CUDA;
+  if (d < 0 || d >= kMaxDevices) return DMUON_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& D = g_dev[d];
+  if (!D.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&D.sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&D.clock_khz, cudaDevAttrClockRate, d) != cudaSuccess)
+      return DMUON_ERR_CUDA;
+    if (major != 10 || minor != 3) {
+      D.status = DMUON_ERR_UNSUPPORTED;
+    } else if (ns_gemm_prepare() != cudaSuccess) {
+      return DMUON_ERR_CUDA;
+    }
+    D.ready = true;
+  }
+  *out = D;
+  return D.status;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_slot_map(CUtensorMap* map, void* base, int cols, int rows, int count, int pitch,
+                     long long stride) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {cuuint64_t(cols), cuuint64_t(rows), cuuint64_t(count)};
+  const cuuint64_t strides[2] = {cuuint64_t(pitch) * 2, cuuint64_t(stride) * 2};
+  const cuuint32_t box[3] = {64, 64, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ------------------------------------------------------------------ one call
+struct Request {
+  int n = 0;
+  const dmuon_shape* shp = nullptr;
+  const void* const* grad = nullptr;
+  int grad_dt = DMUON_BF16;
+  float* const* momentum = nullptr;
+  void* const* weight = nullptr;
+  int weight_dt = DMUON_BF16;
+  const int64_t* offset = nullptr;
+  void* packed = nullptr;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  int variant = DMUON_NS_STANDARD;
+  cudaStream_t stream = nullptr;
+  bool do_pack = false, do_ns = false, do_update = false;
+  float beta = 0.95f;
+  int ns_steps = 5;
+  float abc[3] = {kDefaultAbc[0], kDefaultAbc[1], kDefaultAbc[2]};
+  float eps = kDefaultEps;
+  bool pack_norms = false;
+  float lr = 0.02f;
+};
+
+int check_request(const Request& R, const Plan& P) {
+  if (R.packed == nullptr || R.ws == nullptr || R.offset == nullptr) return DMUON_ERR_INVALID_ARG;
+  if (!aligned(R.packed, 256) || !aligned(R.ws, 256)) return DMUON_ERR_ALIGNMENT;
+  if (R.ws_bytes < P.total) return DMUON_ERR_WORKSPACE;
+  if (R.do_pack) {
+    if (R.grad == nullptr || R.momentum == nullptr) return DMUON_ERR_INVALID_ARG;
+    if (R.grad_dt != DMUON_F32 && R.grad_dt != DMUON_BF16) return DMUON_ERR_INVALID_ARG;
+    if (!std::isfinite(R.beta)) return DMUON_ERR_INVALID_ARG;
+  }
+  if (R.do_update) {
+    if (R.weight == nullptr) return DMUON_ERR_INVALID_ARG;
+    if (R.weight_dt != DMUON_F32 && R.weight_dt != DMUON_BF16) return DMUON_ERR_INVALID_ARG;
+    if (!std::isfinite(R.lr)) return DMUON_ERR_INVALID_ARG;
+  }
+  if (R.do_ns) {
+    if (R.ns_steps < 0 || R.ns_steps > kMaxNsSteps) return DMUON_ERR_INVALID_ARG;
+    if (!(R.eps >= 0.f) || !std::isfinite(R.eps)) return DMUON_ERR_INVALID_ARG;
+    for (float v : R.abc)
+      if (!std::isfinite(v)) return DMUON_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < R.n; ++i) {
+    const bool active = R.shp[i].rows > 0 && R.shp[i].cols > 0;
+    if (!active) continue;
+    if (R.offset[i] < 0 || R.offset[i] % DMUON_PACK_ALIGN_ELEMS != 0) return DMUON_ERR_ALIGNMENT;
+    if (R.do_pack && (R.grad[i] == nullptr || R.momentum[i] == nullptr))
+      return DMUON_ERR_INVALID_ARG;
+    if (R.do_update && R.weight[i] == nullptr) return DMUON_ERR_INVALID_ARG;
+  }
+  return DMUON_OK;
+}
+
+int upload_tables(const Request& R, const Plan& P) {
+  std::vector<unsigned char> blob(P.tables_bytes, 0);
+  unsigned char* ws = static_cast<unsigned char*>(R.ws);
+  auto at = [&](size_t off) { return blob.data() + (off - P.off_tables); };
+  EwMat* ew = reinterpret_cast<EwMat*>(at(P.off_ew));
+  Bucket* bk = reinterpret_cast<Bucket*>(at(P.off_bk));
+  InternalMat* im = reinterpret_cast<InternalMat*>(at(P.off_imat));
+  int* sym = reinterpret_cast<int*>(at(P.off_sym));
+  CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(at(P.off_tmaps));
+
+  for (int i = 0; i < P.n; ++i) {
+    EwMat& E = ew[i];
+    const long long r = R.shp[i].rows, c = R.shp[i].cols;
+    E.rows = int(r);
+    E.cols = int(c);
+    E.numel = r * c;
+    E.active = (r > 0 && c > 0) ? 1 : 0;
+    E.chunk_begin = P.chunk_begin[i];
+    E.tile_begin = P.tile_begin[i];
+    E.n_chunks = P.n_chunks[i];
+    E.tiles_r = P.tiles_r[i];
+    E.tiles_c = P.tiles_c[i];
+    E.packed_off = E.active ? R.offset[i] : 0;
+    E.transposed = r > c ? 1 : 0;
+    E.upd_scale = float(std::sqrt(std::max(1.0, double(r) / double(std::max<long long>(c, 1)))));
+    if (R.do_pack && E.active) {
+      E.g = R.grad[i];
+      E.mom = R.momentum[i];
+      if (aligned(E.g, 16) && aligned(E.mom, 16)) E.flags |= kFlagVecGM;
+    }
+    if (R.do_update && E.active) {
+      E.w = R.weight[i];
+      if (aligned(E.w, 16)) E.flags |= kFlagVecW;
+    }
+    if (c % 8 == 0) E.flags |= kFlagRowsAligned;
+    const int b = P.bucket_of[i];
+    if (b >= 0) {
+      const BucketPlan& B = P.buckets[b];
+      E.pitch_x = B.pitch_x;
+      E.x0 = reinterpret_cast<__nv_bfloat16*>(ws + B.slot_off[SX0]) +
+             (long long)P.idx_in_bucket[i] * B.stride_x;
+      InternalMat& M = im[P.internal_of[i]];
+      M.packed_off = R.offset[i];
+      M.caller = i;
+      M.transposed = E.transposed;
+    }
+  }
+  int sym_off = 0, internal = 0;
+  int sym_begin = 0, full_begin = 0;
+  for (size_t b = 0; b < P.buckets.size(); ++b) {
+    const BucketPlan& BP = P.buckets[b];
+    if (int(b) == P.n_std) sym_begin = full_begin = 0;  // Gram buckets start a new launch group
+    Bucket& B = bk[b];
+    B.m = BP.m;
+    B.n = BP.n;
+    B.count = int(BP.mats.size());
+    B.first = internal;
+    internal += B.count;
+    B.pitch_x = BP.pitch_x;
+    B.pitch_m = BP.pitch_m;
+    B.stride_x = BP.stride_x;
+    B.stride_m = BP.stride_m;
+    B.tmap = int(b) * kSlots;
+    for (int s = 0; s < kSlots; ++s) {
+      if (!BP.used[s]) continue;
+      void* base = ws + BP.slot_off[s];
+      B.slot[s] = static_cast<__nv_bfloat16*>(base);
+      const bool x = slot_is_x(s);
+      if (!encode_slot_map(&maps[b * kSlots + s], base, x ? BP.n : BP.m, BP.m, B.count,
+                           x ? BP.pitch_x : BP.pitch_m, x ? BP.stride_x : BP.stride_m))
+        return DMUON_ERR_CUDA;
+    }
+    B.sym_off = sym_off;
+    B.sym_count = int(BP.sym.size());
+    std::memcpy(sym + sym_off, BP.sym.data(), BP.sym.size() * sizeof(int));
+    sym_off += B.sym_count;
+    B.full_ti = BP.full_ti;
+    B.full_tj = BP.full_tj;
+    B.sym_begin = sym_begin;
+    B.full_begin = full_begin;
+    sym_begin += B.count * B.sym_count;
+    full_begin += B.count * B.full_ti * B.full_tj;
+  }
+  if (launch_upload(ws + P.off_tables, blob.data(), blob.size(), R.stream) != cudaSuccess)
+    return DMUON_ERR_CUDA;
+  return DMUON_OK;
+}
+
+// Total tiles of a launch over buckets [b0, b1).
+void group_tiles(const Plan& P, int b0, int b1, int* sym_tiles, int* full_tiles) {
+  long long s = 0, f = 0;
+  for (int b = b0; b < b1; ++b) {
+    const BucketPlan& B = P.buckets[b];
+    s += (long long)B.mats.size() * B.sym.size();
+    f += (long long)B.mats.size() * B.full_ti * B.full_tj;
+  }
+  *sym_tiles = int(s);
+  *full_tiles = int(f);
+}
+
+struct GemmLauncher {
+  const Plan& P;
+  const Request& R;
+  int sms;
+  unsigned char* ws;
+  int b0 = 0, b1 = 0, sym_tiles = 0, full_tiles = 0;
+
+  GemmArgs base() const {
+    GemmArgs g{};
+    g.buckets = reinterpret_cast<const Bucket*>(ws + P.off_bk) + b0;
+    g.tmaps = ws + P.off_tmaps;
+    g.sym_tiles = reinterpret_cast<const int*>(ws + P.off_sym);
+    g.imat = reinterpret_cast<const InternalMat*>(ws + P.off_imat);
+    g.packed = static_cast<__nv_bfloat16*>(R.packed);
+    g.err = reinterpret_cast<int*>(ws);
+    g.n_buckets = b1 - b0;
+    return g;
+  }
+  // out = alpha*I + beta*aux + gamma*L R^T  (m x m, symmetric)
+  bool sym(int sL, int sR, int sAux, int sOut, float alpha, float beta, float gamma) const {
+    GemmArgs g = base();
+    g.total_tiles = sym_tiles;
+    g.sL = sL; g.sR = sR; g.sAux = sAux; g.sOut = sOut;
+    g.alpha = alpha; g.beta = beta; g.gamma = gamma;
+    return launch_ns_gemm(g, false, sms, R.stream) == cudaSuccess;
+  }
+  // out = alpha*aux + gamma*L R  (m x n); final: write O into the packed buffer
+  bool full(int sL, int sR, int sAux, int sOut, float alpha, float gamma, bool final) const {
+    GemmArgs g = base();
+    g.total_tiles = full_tiles;
+    g.sL = sL; g.sR = sR; g.sAux = sAux; g.sOut = sOut;
+    g.alpha = alpha; g.beta = 0.f; g.gamma = gamma;
+    g.final_out = final ? 1 : 0;
+    return launch_ns_gemm(g, true, sms, R.stream) == cudaSuccess;
+  }
+};
+
+int run(const Request& R) {
+  if (R.n < 0 || (R.n > 0 && R.shp == nullptr)) return DMUON_ERR_INVALID_ARG;
+  Plan P;
+  int st = build_plan(R.n, R.shp, R.variant, P);
+  if (st != DMUON_OK) return st;
+  st = check_request(R, P);
+  if (st != DMUON_OK) return st;
+  if (R.n == 0) return DMUON_OK;
+  DevInfo D;
+  st = device_info(&D);
+  if (st != DMUON_OK) return st;
+  if (tensor_map_encoder() == nullptr) return DMUON_ERR_CUDA;
+  st = upload_tables(R, P);
+  if (st != DMUON_OK) return st;
+
+  unsigned char* ws = static_cast<unsigned char*>(R.ws);
+  const EwMat* ew = reinterpret_cast<const EwMat*>(ws + P.off_ew);
+  float* partials = reinterpret_cast<float*>(ws + P.off_partials);
+  float* inv = reinterpret_cast<float*>(ws + P.off_inv);
+  __nv_bfloat16* packed = static_cast<__nv_bfloat16*>(R.packed);
+  cudaStream_t s = R.stream;
+
+  if (R.do_pack) {
+    if (launch_momentum_pack(ew, R.n, P.total_chunks, R.grad_dt == DMUON_BF16, R.beta, packed,
+                             partials, s) != cudaSuccess)
+      return DMUON_ERR_CUDA;
+  }
+  if (R.do_ns) {
+    if (!R.do_pack && !R.pack_norms) {
+      if (launch_norm_partials(ew, R.n, P.total_chunks, packed, partials, s) != cudaSuccess)
+        return DMUON_ERR_CUDA;
+    }
+    if (launch_norm_finalize(ew, R.n, partials, R.eps, inv, s) != cudaSuccess)
+      return DMUON_ERR_CUDA;
+    if (R.ns_steps == 0) {
+      if (launch_scale_inplace(ew, R.n, P.total_chunks, packed, inv, s) != cudaSuccess)
+        return DMUON_ERR_CUDA;
+    } else {
+      if (launch_relayout(ew, R.n, P.total_tiles, packed, inv, s) != cudaSuccess)
+        return DMUON_ERR_CUDA;
+      const float a = R.abc[0], b = R.abc[1], c = R.abc[2];
+      // standard buckets: per step A = X X^T; B = b A + c A A; X' = a X + B X
+      if (P.n_std > 0) {
+        GemmLauncher L{P, R, D.sms, ws};
+        L.b0 = 0;
+        L.b1 = P.n_std;
+        group_tiles(P, L.b0, L.b1, &L.sym_tiles, &L.full_tiles);
+        for (int k = 0; k < R.ns_steps; ++k) {
+          const int xin = (k & 1) ? SX1 : SX0, xout = (k & 1) ? SX0 : SX1;
+          const bool last = k + 1 == R.ns_steps;
+          if (!L.sym(xin, xin, SM0, SM0, 0.f, 0.f, 1.f)) return DMUON_ERR_CUDA;
+          if (!L.sym(SM0, SM0, SM0, SM1, 0.f, b, c)) return DMUON_ERR_CUDA;
+          if (!L.full(SM1, xin, xin, xout, a, 1.f, last)) return DMUON_ERR_CUDA;
+        }
+      }
+      // Gram buckets: A0 = X0 X0^T; per step P = aI + bA + cA^2, Q = P Q,
+      // A' = A P^2; finally O = Q X0.  Slots: A in SM0/SM1, P in SM2 (SM3 at
+      // step 0, where Q = P), Q in SM3/SM4, T = P^2 in SM5.
+      if (P.n_std < int(P.buckets.size())) {
+        GemmLauncher L{P, R, D.sms, ws};
+        L.b0 = P.n_std;
+        L.b1 = int(P.buckets.size());
+        group_tiles(P, L.b0, L.b1, &L.sym_tiles, &L.full_tiles);
+        int sA = SM0, sAn = SM1, sQ = SM3, sQn = SM4;
+        if (!L.sym(SX0, SX0, SM0, sA, 0.f, 0.f, 1.f)) return DMUON_ERR_CUDA;
+        for (int k = 0; k < R.ns_steps; ++k) {
+          const bool last = k + 1 == R.ns_steps;
+          const int sP = (k == 0) ? SM3 : SM2;
+          if (!L.sym(sA, sA, sA, sP, a, b, c)) return DMUON_ERR_CUDA;
+          if (k > 0) {
+            if (!L.sym(sP, sQ, SM0, sQn, 0.f, 0.f, 1.f)) return DMUON_ERR_CUDA;
+            std::swap(sQ, sQn);
+          }
+          if (!last) {
+            if (!L.sym(sP, sP, SM0, SM5, 0.f, 0.f, 1.f)) return DMUON_ERR_CUDA;
+            if (!L.sym(sA, SM5, SM0, sAn, 0.f, 0.f, 1.f)) return DMUON_ERR_CUDA;
+            std::swap(sA, sAn);
+          }
+        }
+        if (!L.full(sQ, SX0, SX0, SX0, 0.f, 1.f, true)) return DMUON_ERR_CUDA;
+      }
+    }
+  }
+  if (R.do_update) {
+    if (launch_update(ew, R.n, P.total_chunks, R.weight_dt == DMUON_BF16, R.lr, packed, s) !=
+        cudaSuccess)
+      return DMUON_ERR_CUDA;
+  }
+  return DMUON_OK;
+}
+
+}  // namespace
+}  // namespace dm
+
+using namespace dm;
+
+extern "C" {
+
+int dmuon_plan(int n, const dmuon_shape* shp, int n_owners, int* owner_of, int64_t* offset,
+               int64_t* owner_elems) {
+  if (n < 0 || n_owners <= 0) return DMUON_ERR_INVALID_ARG;
+  if (n > 0 && (shp == nullptr || owner_of == nullptr || offset == nullptr))
+    return DMUON_ERR_INVALID_ARG;
+  if (owner_elems == nullptr) return DMUON_ERR_INVALID_ARG;
+  std::vector<int64_t> size(n);
+  for (int i = 0; i < n; ++i) {
+    if (!shape_ok(shp[i])) return DMUON_ERR_INVALID_ARG;
+    size[i] = shp[i].rows * shp[i].cols;
+  }
+  // greedy LPT: descending size (ties: lower index), least-loaded owner (ties: lower owner)
+  std::vector<int> order(n);
+  for (int i = 0; i < n; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return size[a] > size[b]; });
+  std::vector<int64_t> load(n_owners, 0);
+  for (int i : order) {
+    int best = 0;
+    if (n_owners > 1)
+      for (int o = 1; o < n_owners; ++o)
+        if (load[o] < load[best]) best = o;
+    owner_of[i] = n_owners > 1 ? best : 0;
+    load[owner_of[i]] += size[i];
+  }
+  int64_t base = 0;
+  for (int o = 0; o < n_owners; ++o) {
+    int64_t cur = 0;
+    for (int i = 0; i < n; ++i) {
+      if (owner_of[i] != o) continue;
+      offset[i] = base + cur;
+      cur = int64_t(align_up(size_t(cur + size[i]), DMUON_PACK_ALIGN_ELEMS));
+    }
+    owner_elems[o] = cur;
+    base += cur;
+  }
+  return DMUON_OK;
+}
+
+size_t dmuon_workspace_bytes(int n, const dmuon_shape* shp, int ns_variant) {
+  Plan P;
+  if (build_plan(n, shp, ns_variant, P) != DMUON_OK) return 0;
+  return P.total;
+}
+
+int dmuon_pack(int n, const dmuon_shape* shp, const void* const* grad, int grad_dt,
+               float* const* momentum, float beta, void* packed_bf16, const int64_t* offset,
+               void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  Request R;
+  R.n = n; R.shp = shp; R.grad = grad; R.grad_dt = grad_dt; R.momentum = momentum;
+  R.beta = beta; R.packed = packed_bf16; R.offset = offset; R.ws = workspace;
+  R.ws_bytes = ws_bytes; R.stream = stream; R.do_pack = true;
+  return run(R);
+}
+
+int dmuon_ns_batched(int n, const dmuon_shape* shp, void* packed_bf16, const int64_t* offset,
+                     int ns_steps, int ns_variant, const float* abc, float eps,
+                     int use_pack_norms, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  Request R;
+  R.n = n; R.shp = shp; R.packed = packed_bf16; R.offset = offset; R.ns_steps = ns_steps;
+  R.variant = ns_variant;
+  if (abc != nullptr) { R.abc[0] = abc[0]; R.abc[1] = abc[1]; R.abc[2] = abc[2]; }
+  R.eps = eps; R.pack_norms = use_pack_norms != 0; R.ws = workspace; R.ws_bytes = ws_bytes;
+  R.stream = stream; R.do_ns = true;
+  return run(R);
+}
+
+int dmuon_unpack_update(int n, const dmuon_shape* shp, void* const* weight, int weight_dt,
+                        float lr, const void* packed_bf16, const int64_t* offset, void* workspace,
+                        size_t ws_bytes, cudaStream_t stream) {
+  Request R;
+  R.n = n; R.shp = shp; R.weight = weight; R.weight_dt = weight_dt; R.lr = lr;
+  R.packed = const_cast<void*>(packed_bf16); R.offset = offset; R.ws = workspace;
+  R.ws_bytes = ws_bytes; R.stream = stream; R.do_update = true;
+  return run(R);
+}
+
+int dmuon_muon_step(int n, const dmuon_shape* shp, const void* const* grad, int grad_dt,
+                    float* const* momentum, void* const* weight, int weight_dt, float lr,
+                    float beta, int ns_steps, int ns_variant, void* packed_bf16,
+                    const int64_t* offset, void* workspace, size_t ws_bytes,
+                    cudaStream_t stream) {
+  Request R;
+  R.n = n; R.shp = shp; R.grad = grad; R.grad_dt = grad_dt; R.momentum = momentum;
+  R.weight = weight; R.weight_dt = weight_dt; R.lr = lr; R.beta = beta; R.ns_steps = ns_steps;
+  R.variant = ns_variant; R.packed = packed_bf16; R.offset = offset; R.ws = workspace;
+  R.ws_bytes = ws_bytes; R.stream = stream;
+  R.do_pack = R.do_ns = R.do_update = true;
+  R.pack_norms = true;
+  return run(R);
+}
+
+int dmuon_stream_status(cudaStream_t stream, void* workspace) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DMUON_ERR_CUDA;
+  if (workspace == nullptr) return DMUON_OK;
+  if (!aligned(workspace, 256)) return DMUON_ERR_ALIGNMENT;
+  int err = 0;
+  if (cudaMemcpyAsync(&err, workspace, sizeof(int), cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return DMUON_ERR_CUDA;
+  if (err != 0) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+      return DMUON_ERR_CUDA;
+    return err;
+  }
+  return DMUON_OK;
+}
+
+int dmuon_debug_wait_timeout(void* workspace, size_t ws_bytes, int budget_us,
+                             cudaStream_t stream) {
+  if (workspace == nullptr || ws_bytes < kHdrBytes) return DMUON_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return DMUON_ERR_ALIGNMENT;
+  if (budget_us < 1 || budget_us > 1000000) return DMUON_ERR_INVALID_ARG;
+  DevInfo D;
+  const int st = device_info(&D);
+  if (st != DMUON_OK) return st;
+  const long long cycles = (long long)budget_us * (long long)D.clock_khz / 1000;
+  if (launch_wait_timeout(static_cast<int*>(workspace), cycles, stream) != cudaSuccess)
+    return DMUON_ERR_CUDA;
+  return DMUON_OK;
+}
+
+const char* dmuon_status_string(int status) {
+  switch (status) {
+    case DMUON_OK: return "ok";
+    case DMUON_ERR_INVALID_ARG: return "invalid argument";
+    case DMUON_ERR_ALIGNMENT: return "misaligned pointer or offset";
+    case DMUON_ERR_WORKSPACE: return "workspace too small";
+    case DMUON_ERR_CUDA: return "CUDA error";
+    case DMUON_ERR_TIMEOUT: return "bounded device wait timed out";
+    case DMUON_ERR_UNSUPPORTED: return "unsupported device or shape";
+    default: return "unknown status";
+  }
+}
+
+int dmuon_version(void) { return 100; }
+
+}  // extern "C"

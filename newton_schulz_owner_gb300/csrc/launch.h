@@ -1,0 +1,34 @@
+// Host-side launchers shared between the C-ABI layer and the kernel files.
+#pragma once
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "tables.h"
+
+namespace dm {
+
+// ns_gemm.cu
+size_t ns_gemm_smem_bytes();
+cudaError_t ns_gemm_prepare();  // once per device: opt into large shared memory
+cudaError_t launch_ns_gemm(const GemmArgs& g, bool full, int num_sms, cudaStream_t s);
+
+// elementwise.cu
+// Copy `bytes` (multiple of 16) from host memory into device memory through
+// kernel parameters (stream-ordered, no host staging, no allocation).
+cudaError_t launch_upload(void* dst, const void* src, size_t bytes, cudaStream_t s);
+cudaError_t launch_momentum_pack(const EwMat* ew, int n, long long total_chunks, bool grad_bf16,
+                                 float beta, __nv_bfloat16* packed, float* partials,
+                                 cudaStream_t s);
+cudaError_t launch_norm_partials(const EwMat* ew, int n, long long total_chunks,
+                                 const __nv_bfloat16* packed, float* partials, cudaStream_t s);
+cudaError_t launch_norm_finalize(const EwMat* ew, int n, const float* partials, float eps,
+                                 float* inv_norm, cudaStream_t s);
+cudaError_t launch_relayout(const EwMat* ew, int n, long long total_tiles,
+                            const __nv_bfloat16* packed, const float* inv_norm, cudaStream_t s);
+cudaError_t launch_scale_inplace(const EwMat* ew, int n, long long total_chunks,
+                                 __nv_bfloat16* packed, const float* inv_norm, cudaStream_t s);
+cudaError_t launch_update(const EwMat* ew, int n, long long total_chunks, bool weight_bf16,
+                          float lr, const __nv_bfloat16* packed, cudaStream_t s);
+cudaError_t launch_wait_timeout(int* err, long long budget_cycles, cudaStream_t s);
+
+}  // namespace dm

@@ -1,0 +1,437 @@
+// Grouped, persistent tcgen05 GEMM for the Newton-Schulz products.
+//
+// One launch runs one product for every matrix of every bucket:
+//   symmetric:  out = alpha*I + beta*aux + gamma * L R^T   (m x m, upper-triangle
+//               tiles only, each tile also stored mirrored)
+//               X X^T      -> L = R = X (K = n)
+//               A A        -> L = R = A, aux = A (B = b*A + c*A*A)
+//   full:       out = alpha*aux + gamma * L R              (m x n)
+//               B X        -> L = B, R = X, aux = X  (X' = a*X + B*X)
+// The standard Muon iteration is these three launches per step; the Gram
+// variant chains symmetric launches on m x m matrices.
+//
+// CTA layout (320 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer: 128x64 tile of L and 256x64 tile of R per stage,
+//               128-byte swizzle, 4-stage ring of shared memory
+//   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
+//               (M=128, N=256, K=16) into one of two 256-column accumulators
+//   warps 2-9   epilogue: tcgen05.ld, fused polynomial / axpy, bf16 stores
+// Tiles are handed out statically (tile = blockIdx.x + k * gridDim.x), so each
+// role walks the same sequence without talking to the others.
+#include "dmuon.h"
+#include "launch.h"
+#include "ptx.cuh"
+#include "tables.h"
+
+#include <cuda_bf16.h>
+
+namespace dm {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kAStage = kBM * kBK * 2;  // 16 KB
+constexpr int kBStage = kBN * kBK * 2;  // 32 KB
+constexpr int kStageBytes = kAStage + kBStage;
+constexpr int kBox = 64 * 64 * 2;       // one TMA box: 64 rows x 128 bytes
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kTmemCols = 512;
+constexpr int kAccCols = 256;
+constexpr int kBarBytes = 256;
+constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 + kBarBytes;
+
+struct TileInfo {
+  int bucket, mat, ti, tj;
+};
+
+template <bool FULL>
+DM_DEV TileInfo decode_tile(const GemmArgs& g, int t) {
+  int lo = 0, hi = g.n_buckets - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    const int b = FULL ? g.buckets[mid].full_begin : g.buckets[mid].sym_begin;
+    if (b <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const Bucket& B = g.buckets[lo];
+  TileInfo T;
+  T.bucket = lo;
+  if (FULL) {
+    // column-panel major: consecutive tiles share the R (= X) column panel
+    const int local = t - B.full_begin;
+    const int per = B.full_ti * B.full_tj;
+    T.mat = local / per;
+    const int r = local - T.mat * per;
+    T.tj = r / B.full_ti;
+    T.ti = r - T.tj * B.full_ti;
+  } else {
+    const int local = t - B.sym_begin;
+    T.mat = local / B.sym_count;
+    const int r = local - T.mat * B.sym_count;
+    const int p = g.sym_tiles[B.sym_off + r];
+    T.ti = p >> 16;
+    T.tj = p & 0xFFFF;
+  }
+  return T;
+}
+
+template <bool FULL>
+DM_DEV int k_extent(const GemmArgs& g, const Bucket& B) {
+  if (FULL) return B.m;
+  return slot_is_x(g.sL) ? B.n : B.m;
+}
+
+DM_DEV const void* tmap_of(const GemmArgs& g, const Bucket& B, int slot) {
+  return g.tmaps + size_t(B.tmap + slot) * 128;
+}
+
+DM_DEV void raise_abort(int* err, volatile int* abort_flag) {
+  *abort_flag = 1;
+  atomicCAS(err, 0, int(DMUON_ERR_TIMEOUT));
+}
+
+DM_DEV uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+
+DM_DEV void load_bf16x32(const __nv_bfloat16* p, float (&f)[32]) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 u = q[v];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+      const float2 f2 = __bfloat1622float2(b2);
+      f[v * 8 + 2 * k] = f2.x;
+      f[v * 8 + 2 * k + 1] = f2.y;
+    }
+  }
+}
+
+DM_DEV void store_bf16x32(__nv_bfloat16* p, const float (&f)[32]) {
+  uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    uint4 u;
+    u.x = pack_bf16x2(f[v * 8 + 0], f[v * 8 + 1]);
+    u.y = pack_bf16x2(f[v * 8 + 2], f[v * 8 + 3]);
+    u.z = pack_bf16x2(f[v * 8 + 4], f[v * 8 + 5]);
+    u.w = pack_bf16x2(f[v * 8 + 6], f[v * 8 + 7]);
+    q[v] = u;
+  }
+}
+
+// ------------------------------------------------------------------ roles
+template <bool FULL>
+DM_DEV void producer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* full_bar,
+                     uint64_t* empty_bar, volatile int* abort_flag) {
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t issued = 0, last_parity = 0;
+  int prev_bucket = -1;
+  for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x) {
+    const TileInfo T = decode_tile<FULL>(g, t);
+    const Bucket& B = g.buckets[T.bucket];
+    const void* mapL = tmap_of(g, B, g.sL);
+    const void* mapR = tmap_of(g, B, g.sR);
+    if (T.bucket != prev_bucket) {
+      tensormap_acquire(mapL);
+      tensormap_acquire(mapR);
+      prev_bucket = T.bucket;
+    }
+    const int KB = (k_extent<FULL>(g, B) + kBK - 1) / kBK;
+    const int row0 = T.ti * kBM;
+    const int col0 = T.tj * kBN;
+    for (int kb = 0; kb < KB; ++kb) {
+      if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+        raise_abort(g.err, abort_flag);
+        goto drain;
+      }
+      mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
+      {
+        uint8_t* a = sA + stage * kAStage;
+        uint8_t* b = sB + stage * kBStage;
+        const int k0 = kb * kBK;
+        tma_load_3d(a, mapL, &full_bar[stage], k0, row0, T.mat);
+        tma_load_3d(a + kBox, mapL, &full_bar[stage], k0, row0 + 64, T.mat);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (FULL)  // R = X, MN-major: 64 K-rows x 64 columns per box
+            tma_load_3d(b + q * kBox, mapR, &full_bar[stage], col0 + 64 * q, k0, T.mat);
+          else       // R rows, K-major
+            tma_load_3d(b + q * kBox, mapR, &full_bar[stage], k0, col0 + 64 * q, T.mat);
+        }
+      }
+      issued |= 1u << stage;
+      last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+drain:
+  // Never leave with bulk copies still landing in shared memory.
+  for (int s = 0; s < kStages; ++s)
+    if (issued & (1u << s)) (void)mbar_wait(&full_bar[s], (last_parity >> s) & 1u, nullptr);
+}
+
+template <bool FULL>
+DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* full_bar,
+                       uint64_t* empty_bar, uint64_t* tfull, uint64_t* tempty,
+                       uint64_t* drain_bar, uint32_t tmem_base, volatile int* abort_flag) {
+  constexpr uint32_t idesc = idesc_bf16(kBM, kBN, FULL);
+  const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+  int stage = 0;
+  uint32_t phase = 0;
+  int it = 0;
+  for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x, ++it) {
+    const TileInfo T = decode_tile<FULL>(g, t);
+    const Bucket& B = g.buckets[T.bucket];
+    const int KB = (k_extent<FULL>(g, B) + kBK - 1) / kBK;
+    const int acc = it & 1;
+    const uint32_t aph = uint32_t(it >> 1) & 1u;
+    if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag)) {
+      raise_abort(g.err, abort_flag);
+      break;
+    }
+    tc_fence_after();
+    const uint32_t d = tmem_base + uint32_t(acc * kAccCols);
+    bool ok = true;
+    for (int kb = 0; kb < KB; ++kb) {
+      if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+        raise_abort(g.err, abort_flag);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sa = a0 + uint32_t(stage * kAStage);
+      const uint32_t sb = b0 + uint32_t(stage * kBStage);
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k) {
+        // K-major L: 16 K-elements = 32 bytes along the swizzled 128-byte row;
+        // 8-row groups 1024 bytes apart.
+        const uint64_t ad = sdesc_sw128(sa + uint32_t(k * 32), 16, 1024);
+        // MN-major R: 64-column atoms 8 KB apart (LBO), 8-row K groups 1 KB
+        // apart (SBO); 16 K-rows = 2 KB.  K-major R as for L.
+        const uint64_t bd = FULL ? sdesc_sw128(sb + uint32_t(k * 2048), kBox, 1024)
+                                 : sdesc_sw128(sb + uint32_t(k * 32), 16, 1024);
+        umma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+      }
+      umma_commit(&empty_bar[stage]);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) break;
+    umma_commit(&tfull[acc]);
+  }
+  // Every issued MMA must finish before TMEM and shared memory go away.
+  umma_commit(drain_bar);
+  (void)mbar_wait(drain_bar, 0, nullptr);
+}
+
+template <bool FULL>
+DM_DEV void store_tile_chunk(const GemmArgs& g, const Bucket& B, const TileInfo& T, int r,
+                             int c0, const float (&acc)[32]) {
+  float o[32];
+  if (!FULL) {
+    const int m = B.m;
+    const int pm = B.pitch_m;
+    __nv_bfloat16* out = B.slot[g.sOut] + (long long)T.mat * B.stride_m;
+    if (g.beta != 0.f) {
+      float a[32];
+      load_bf16x32(B.slot[g.sAux] + (long long)T.mat * B.stride_m + (long long)r * pm + c0, a);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = fmaf(g.gamma, acc[j], g.beta * a[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = g.gamma * acc[j];
+    }
+    if (g.alpha != 0.f) {
+      const int d = r - c0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j == d) o[j] += g.alpha;
+    }
+    __nv_bfloat16* row = out + (long long)r * pm;
+    if (c0 >= r && c0 + 32 <= m) {
+      store_bf16x32(row + c0, o);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int col = c0 + j;
+        if (col >= r && col < m) row[col] = __float2bfloat16_rn(o[j]);
+      }
+    }
+    // mirror: lanes hold consecutive rows, so each store is one 64-byte run
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int col = c0 + j;
+      if (col > r && col < m) out[(long long)col * pm + r] = __float2bfloat16_rn(o[j]);
+    }
+  } else {
+    const int m = B.m, n = B.n;
+    if (g.alpha != 0.f) {
+      float x[32];
+      load_bf16x32(B.slot[g.sAux] + (long long)T.mat * B.stride_x + (long long)r * B.pitch_x + c0,
+                   x);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = fmaf(g.gamma, acc[j], g.alpha * x[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = g.gamma * acc[j];
+    }
+    if (!g.final_out) {
+      __nv_bfloat16* row =
+          B.slot[g.sOut] + (long long)T.mat * B.stride_x + (long long)r * B.pitch_x;
+      if (c0 + 32 <= n) {
+        store_bf16x32(row + c0, o);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < n) row[c0 + j] = __float2bfloat16_rn(o[j]);
+      }
+    } else {
+      const InternalMat im = g.imat[B.first + T.mat];
+      __nv_bfloat16* P = g.packed + im.packed_off;
+      if (!im.transposed) {
+        __nv_bfloat16* row = P + (long long)r * n;
+        if ((n & 7) == 0 && c0 + 32 <= n) {
+          store_bf16x32(row + c0, o);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c0 + j < n) row[c0 + j] = __float2bfloat16_rn(o[j]);
+        }
+      } else {
+        // parameter is (n, m): element (r, c) of X goes to row c, column r
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < n) P[(long long)(c0 + j) * m + r] = __float2bfloat16_rn(o[j]);
+      }
+    }
+  }
+}
+
+template <bool FULL>
+DM_DEV void epilogue(const GemmArgs& g, uint64_t* tfull, uint64_t* tempty, uint32_t tmem_base,
+                     volatile int* abort_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;          // TMEM lane quarter this warp may read
+  const int h = (warp - 2) >> 2;   // which 128-column half of the tile
+  int it = 0;
+  for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x, ++it) {
+    const TileInfo T = decode_tile<FULL>(g, t);
+    const Bucket& B = g.buckets[T.bucket];
+    const int acc = it & 1;
+    const uint32_t aph = uint32_t(it >> 1) & 1u;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(&tfull[acc], aph, abort_flag) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) raise_abort(g.err, abort_flag);
+      break;
+    }
+    tc_fence_after();
+    const int r = T.ti * kBM + q * 32 + lane;
+    const int ncols = FULL ? B.n : B.m;
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      const int tcol = h * 128 + cc * 32;
+      const int c0 = T.tj * kBN + tcol;
+      if (c0 >= ncols) break;  // warp-uniform
+      float v[32];
+      tmem_ld32(tmem_base + uint32_t(acc * kAccCols + tcol) + (uint32_t(q * 32) << 16), v);
+      tmem_ld_wait();
+      if (r < B.m) store_tile_chunk<FULL>(g, B, T, r, c0, v);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tempty[acc]);
+  }
+}
+
+template <bool FULL>
+__global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kAStage;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sB + kStages * kBStage);
+  uint64_t* empty_bar = full_bar + kStages;
+  uint64_t* tfull = empty_bar + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain_bar = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (threadIdx.x == 0) {
+    producer<FULL>(g, sA, sB, full_bar, empty_bar, abort_flag);
+  } else if (threadIdx.x == 32) {
+    mma_issuer<FULL>(g, sA, sB, full_bar, empty_bar, tfull, tempty, drain_bar, tmem_base,
+                     abort_flag);
+  } else if (warp >= 2) {
+    epilogue<FULL>(g, tfull, tempty, tmem_base, abort_flag);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t ns_gemm_smem_bytes() { return kSmemBytes; }
+
+cudaError_t ns_gemm_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(ns_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(kSmemBytes));
+}
+
+cudaError_t launch_ns_gemm(const GemmArgs& g, bool full, int num_sms, cudaStream_t s) {
+  if (g.total_tiles <= 0 || g.n_buckets <= 0) return cudaSuccess;
+  const int grid = g.total_tiles < num_sms ? g.total_tiles : num_sms;
+  if (full)
+    ns_gemm_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(g);
+  else
+    ns_gemm_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(g);
+  return cudaGetLastError();
+}
+
+}  // namespace dm

@@ -1,0 +1,92 @@
+// Device-side tables that the host planner writes into the caller's
+// workspace and the kernels read.  Plain-old-data only.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+
+namespace dm {
+
+// Elementwise kernels (momentum + pack, norm partials, update) walk each
+// matrix in chunks of kChunk elements; one block per chunk.
+constexpr int kChunk = 8192;
+constexpr int kEwThreads = 256;
+// Relayout (normalise + optional transpose into the working layout): 64x64 tiles.
+constexpr int kRelayTile = 64;
+
+// Per-bucket buffers.  Slots 0-1 hold m x n working matrices X, slots 2-7 hold
+// m x m matrices (A, B for standard Newton-Schulz; A, P, Q, T for Gram).
+constexpr int kSlots = 8;
+enum Slot : int { SX0 = 0, SX1 = 1, SM0 = 2, SM1 = 3, SM2 = 4, SM3 = 5, SM4 = 6, SM5 = 7 };
+__host__ __device__ constexpr bool slot_is_x(int s) { return s < 2; }
+
+// EwMat::flags
+constexpr int kFlagVecGM = 1;      // grad, momentum 16-byte aligned
+constexpr int kFlagVecW = 2;       // weight 16-byte aligned
+constexpr int kFlagRowsAligned = 4;  // cols % 8 == 0: packed rows 16-byte aligned
+
+// One entry per caller matrix, in the caller's order.
+struct EwMat {
+  const void* g;           // gradient (bf16 or fp32)
+  float* mom;              // momentum (fp32)
+  void* w;                 // weight (bf16 or fp32)
+  __nv_bfloat16* x0;       // working-layout destination (bucket slot 0)
+  long long packed_off;    // element offset of the packed segment
+  long long numel;         // rows * cols
+  long long chunk_begin;   // first elementwise chunk
+  long long tile_begin;    // first relayout tile
+  int rows, cols;
+  int n_chunks;
+  int tiles_r, tiles_c;    // relayout tile grid over (rows, cols)
+  int pitch_x;             // row pitch of the working layout (elements)
+  int transposed;          // rows > cols: working matrix is the transpose
+  int flags;
+  float upd_scale;         // sqrt(max(1, rows / cols))
+  int active;              // 0 for empty matrices (rows or cols == 0)
+};
+
+// Matrices with the same working shape (m, n) form a bucket; each bucket's
+// buffers hold `count` matrices back to back at a fixed stride, so one 3-D
+// tensor map per buffer covers the whole bucket.
+struct Bucket {
+  int m, n, count, first;        // first: internal index of the bucket's first matrix
+  int pitch_x, pitch_m;          // row pitch (elements) of X slots / m x m slots
+  long long stride_x, stride_m;  // elements between consecutive matrices
+  __nv_bfloat16* slot[kSlots];   // base of each slot (null if unused)
+  int tmap;                      // index of the bucket's first tensor map (kSlots maps)
+  int sym_off, sym_count;        // upper-triangle tile list of an m x m product
+  int full_ti, full_tj;          // tile grid of an m x n product
+  int sym_begin;                 // first tile of this bucket in a symmetric launch
+  int full_begin;                // first tile of this bucket in a full launch
+  int pad_;
+};
+
+// Internal (bucket-major) order -> caller matrix.
+struct InternalMat {
+  long long packed_off;
+  int caller;
+  int transposed;
+};
+
+// Tile shape of the Newton-Schulz products.
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+
+// Launch arguments of the grouped Newton-Schulz product kernel.
+//   symmetric product (m x m output, upper-triangle tiles, mirrored):
+//     out = alpha * I + beta * aux + gamma * (L R^T)
+//   full product (m x n output):
+//     out = alpha * aux + gamma * (L R)        (L: m x m, R: m x n)
+struct GemmArgs {
+  const Bucket* buckets;
+  const unsigned char* tmaps;    // CUtensorMap array, 128 bytes each
+  const int* sym_tiles;          // (ti << 16) | tj
+  const InternalMat* imat;
+  __nv_bfloat16* packed;
+  int* err;
+  int n_buckets;
+  int total_tiles;
+  int sL, sR, sAux, sOut;
+  int final_out;                 // full product: write O into `packed`
+  float alpha, beta, gamma;
+};
+
+}  // namespace dm

@@ -1,0 +1,296 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances (each derived from the arithmetic):
+  * momentum, update (fp32 math): relative Frobenius error <= 1e-5
+  * packed U, bf16 weights: within 1 bf16 ulp of RNE of the fp64 value (the
+    fp32 result can sit on the other side of a rounding boundary)
+  * ns_steps = 0 (normalisation only): <= 5e-3 relative Frobenius (two bf16
+    roundings of at most 2^-9 each)
+  * Newton-Schulz with bf16 operands, fp32 accumulation: <= 2e-2 relative
+    Frobenius per matrix for ns_steps <= 5, 4e-2 for 8 steps
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+NS_TOL = {0: 5e-3, 1: 2e-2, 2: 2e-2, 3: 2e-2, 5: 2e-2, 8: 4e-2}
+
+ODD_SHAPES = [(1, 1), (1, 5), (5, 1), (7, 300), (300, 7), (129, 257), (257, 129), (64, 64),
+              (256, 1024), (1024, 256), (1000, 1000), (96, 4096), (130, 130), (8, 8200),
+              (333, 1500)]
+
+
+@pytest.fixture(scope="module")
+def dm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from newton_schulz_owner_gb300 import build_lib
+    import os
+    if not os.path.exists(build_lib.LIB):
+        build_lib.build()
+    from newton_schulz_owner_gb300 import dmuon
+    return dmuon
+
+
+@pytest.fixture(scope="module")
+def wl():
+    from newton_schulz_owner_gb300 import workloads
+    return workloads
+
+
+def rel(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (nb if nb > 0 else 1.0))
+
+
+def np64(t):
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def bf16_ulp_dist(gpu_bf16: torch.Tensor, ref64: np.ndarray) -> int:
+    """Max distance in bf16 ulps between a bf16 tensor and RNE(ref64)."""
+    ref = torch.from_numpy(oracle.round_bf16(ref64)).to(torch.bfloat16)
+    a = gpu_bf16.detach().cpu().view(torch.int16).to(torch.int32)
+    b = ref.view(torch.int16).to(torch.int32)
+    # map sign-magnitude to a monotone integer line
+    a = torch.where(a < 0, -(a & 0x7FFF), a)
+    b = torch.where(b < 0, -(b & 0x7FFF), b)
+    return int((a - b).abs().max().item()) if a.numel() else 0
+
+
+class PackedSet:
+    """Packed buffer + workspace for a shape list, with canary guards."""
+
+    def __init__(self, dm, shapes, variant=0, guard=True, n_owners=1):
+        self.shapes = shapes
+        own, off, oel = dm.plan(shapes, n_owners)
+        g = 128 if guard else 0
+        # shift every segment by a guard gap so that stray writes land in canaries
+        self.offsets = [o + g * (i + 1) for i, o in enumerate(off)]
+        total = sum(oel) + g * (len(shapes) + 2)
+        self.packed = torch.empty(max(total, 128), dtype=torch.bfloat16, device="cuda")
+        self.canary = torch.tensor([0x7F7F], dtype=torch.int16).view(torch.bfloat16).item()
+        self.packed.fill_(self.canary)
+        self.ws_bytes = dm.workspace_bytes(shapes, variant)
+        self.ws_full = torch.zeros(self.ws_bytes + 4096, dtype=torch.uint8, device="cuda")
+        self.ws_full[self.ws_bytes:] = 0xA5
+        self.workspace = self.ws_full[:self.ws_bytes]
+
+    def view(self, i):
+        r, c = self.shapes[i]
+        o = self.offsets[i]
+        return self.packed[o:o + r * c].view(r, c)
+
+    def guards_intact(self):
+        mask = torch.ones_like(self.packed, dtype=torch.bool)
+        for i, (r, c) in enumerate(self.shapes):
+            mask[self.offsets[i]:self.offsets[i] + r * c] = False
+        bad = (self.packed[mask].view(torch.int16) != 0x7F7F).sum().item()
+        tail = (self.ws_full[self.ws_bytes:] != 0xA5).sum().item()
+        return bad == 0 and tail == 0
+
+
+def run_ns(dm, ps, steps, variant=0, abc=None):
+    dm.ns_batched(ps.shapes, ps.packed, ps.offsets, ps.workspace, ns_steps=steps,
+                  variant=variant, abc=abc, ws_bytes=ps.ws_bytes)
+    assert dm.stream_status(ps.workspace) == dm.OK
+
+
+# ------------------------------------------------------------------ NS
+@pytest.mark.parametrize("steps", [0, 1, 5])
+def test_ns_batched_odd_shapes(dm, wl, steps):
+    ps = PackedSet(dm, ODD_SHAPES)
+    ins = []
+    for i, s in enumerate(ODD_SHAPES):
+        u = wl.random_matrix(s, 100 + i, "cuda", 1.0, torch.bfloat16)
+        ps.view(i).copy_(u)
+        ins.append(np64(u))
+    run_ns(dm, ps, steps)
+    assert ps.guards_intact()
+    for i, s in enumerate(ODD_SHAPES):
+        ref = oracle.newton_schulz(ins[i], steps)
+        err = rel(np64(ps.view(i)), ref)
+        assert err <= NS_TOL[steps], f"{s} steps={steps}: rel err {err:.3e}"
+
+
+def test_ns_phase_isolation(dm, wl):
+    """abc = (1,0,0) returns X0; (0,1,0) gives X0 X0^T X0; (0,0,1) gives (X0 X0^T)^2 X0.
+    Separates the symmetric products and the full product when one is wrong."""
+    shapes = [(256, 1024), (1024, 256), (129, 257), (300, 7)]
+    for abc in ((1.0, 0.0, 0.0), (0.0, 1.0, 0.0), (0.0, 0.0, 1.0)):
+        ps = PackedSet(dm, shapes)
+        ins = []
+        for i, s in enumerate(shapes):
+            u = wl.random_matrix(s, 7 + i, "cuda", 1.0, torch.bfloat16)
+            ps.view(i).copy_(u)
+            ins.append(np64(u))
+        run_ns(dm, ps, 1, abc=abc)
+        for i, s in enumerate(shapes):
+            ref = oracle.newton_schulz(ins[i], 1, abc=abc)
+            err = rel(np64(ps.view(i)), ref)
+            assert err <= 2e-2, f"abc={abc} {s}: rel err {err:.3e}"
+
+
+def test_ns_eight_steps_band(dm, wl):
+    shapes = [(256, 1024), (512, 512)]
+    ps = PackedSet(dm, shapes)
+    ins = []
+    for i, s in enumerate(shapes):
+        u = wl.random_matrix(s, 300 + i, "cuda", 1.0, torch.bfloat16)
+        ps.view(i).copy_(u)
+        ins.append(np64(u))
+    run_ns(dm, ps, 8)
+    for i, s in enumerate(shapes):
+        out = np64(ps.view(i))
+        assert rel(out, oracle.newton_schulz(ins[i], 8)) <= NS_TOL[8]
+        sv = np.linalg.svd(out, compute_uv=False)
+        assert sv.max() <= 1.2025 * 1.02
+
+
+def test_ns_deterministic(dm, wl):
+    shapes = [(1000, 1000), (300, 7), (256, 1024)]
+    outs = []
+    for _ in range(2):
+        ps = PackedSet(dm, shapes)
+        for i, s in enumerate(shapes):
+            ps.view(i).copy_(wl.random_matrix(s, 55 + i, "cuda", 1.0, torch.bfloat16))
+        run_ns(dm, ps, 5)
+        outs.append(ps.packed.clone())
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_ns_zero_matrix_gives_zero(dm):
+    shapes = [(64, 200), (200, 64)]
+    ps = PackedSet(dm, shapes)
+    for i in range(2):
+        ps.view(i).zero_()
+    run_ns(dm, ps, 5)
+    for i in range(2):
+        assert not torch.any(ps.view(i).float() != 0)
+
+
+@pytest.mark.parametrize("steps", [1, 3, 5])
+def test_gram_variant(dm, wl, steps):
+    shapes = [(128, 512), (512, 128), (200, 900), (64, 4096), (300, 300), (7, 300)]
+    ps = PackedSet(dm, shapes, variant=dm.NS_GRAM)
+    ins = []
+    for i, s in enumerate(shapes):
+        u = wl.random_matrix(s, 900 + i, "cuda", 1.0, torch.bfloat16)
+        ps.view(i).copy_(u)
+        ins.append(np64(u))
+    run_ns(dm, ps, steps, variant=dm.NS_GRAM)
+    assert ps.guards_intact()
+    for i, s in enumerate(shapes):
+        m, n = min(s), max(s)
+        ref = (oracle.gram_newton_schulz if n >= 2 * m else oracle.newton_schulz)(ins[i], steps)
+        err = rel(np64(ps.view(i)), ref)
+        assert err <= NS_TOL[steps], f"gram {s} steps={steps}: rel err {err:.3e}"
+
+
+# ------------------------------------------------------------------ pack / update
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
+def test_pack_momentum(dm, wl, gdt):
+    shapes = [(256, 1024), (300, 7), (7, 300), (1, 1), (129, 257)]
+    ps = PackedSet(dm, shapes)
+    grads = [wl.random_matrix(s, 40 + i, "cuda", 1e-3, gdt) for i, s in enumerate(shapes)]
+    moms = [wl.random_matrix(s, 60 + i, "cuda", 1e-3, torch.float32) for i, s in enumerate(shapes)]
+    m0 = [np64(m) for m in moms]
+    dm.pack(shapes, grads, moms, 0.95, ps.packed, ps.offsets, ps.workspace)
+    assert dm.stream_status(ps.workspace) == dm.OK
+    assert ps.guards_intact()
+    for i, s in enumerate(shapes):
+        m_ref, u_ref = oracle.nesterov_momentum(np64(grads[i]), m0[i], 0.95)
+        assert rel(np64(moms[i]), m_ref) <= 1e-5
+        assert bf16_ulp_dist(ps.view(i), u_ref) <= 1
+
+
+def test_pack_then_ns_uses_fp32_norm(dm, wl):
+    shapes = [(256, 1024), (1024, 256)]
+    ps = PackedSet(dm, shapes)
+    grads = [wl.random_matrix(s, 70 + i, "cuda", 1.0, torch.float32) for i, s in enumerate(shapes)]
+    moms = [torch.zeros(s, device="cuda") for s in shapes]
+    dm.pack(shapes, grads, moms, 0.95, ps.packed, ps.offsets, ps.workspace)
+    dm.ns_batched(shapes, ps.packed, ps.offsets, ps.workspace, ns_steps=0, use_pack_norms=True,
+                  ws_bytes=ps.ws_bytes)
+    assert dm.stream_status(ps.workspace) == dm.OK
+    for i, s in enumerate(shapes):
+        _, u = oracle.nesterov_momentum(np64(grads[i]), np.zeros(s), 0.95)
+        assert rel(np64(ps.view(i)), oracle.newton_schulz(u, 0)) <= 5e-3
+
+
+@pytest.mark.parametrize("wdt", [torch.float32, torch.bfloat16])
+def test_unpack_update(dm, wl, wdt):
+    shapes = [(256, 1024), (1024, 256), (300, 7), (3, 3)]
+    ps = PackedSet(dm, shapes)
+    for i, s in enumerate(shapes):
+        ps.view(i).copy_(wl.random_matrix(s, 80 + i, "cuda", 0.03, torch.bfloat16))
+    ws = [wl.random_matrix(s, 90 + i, "cuda", 0.02, wdt) for i, s in enumerate(shapes)]
+    w0 = [np64(w) for w in ws]
+    dm.unpack_update(shapes, ws, 0.02, ps.packed, ps.offsets, ps.workspace)
+    assert dm.stream_status(ps.workspace) == dm.OK
+    for i, s in enumerate(shapes):
+        ref = oracle.apply_update(w0[i], np64(ps.view(i)), 0.02)
+        if wdt == torch.float32:
+            assert rel(np64(ws[i]) - w0[i], ref - w0[i]) <= 1e-5
+        else:
+            assert bf16_ulp_dist(ws[i], ref) <= 1
+
+
+# ------------------------------------------------------------------ whole step
+def _muon_case(dm, wl, shapes, gdt, wdt, steps=2, variant=0, seed=0, ns_steps=5):
+    from newton_schulz_owner_gb300.dmuon import MuonOwner
+    own = MuonOwner(shapes, variant=variant)
+    ws = [wl.random_matrix(s, seed + 500 + i, "cuda", 0.02, wdt) for i, s in enumerate(shapes)]
+    ms = [torch.zeros(s, device="cuda") for s in shapes]
+    m_ref = [np.zeros(s) for s in shapes]
+    w_ref = [np64(w) for w in ws]
+    worst = 0.0
+    for step in range(steps):
+        gs = [wl.random_matrix(s, seed + 1000 * step + i, "cuda", 1e-3 if gdt == torch.bfloat16
+                               else 1.0, gdt) for i, s in enumerate(shapes)]
+        w_before = [np64(w) for w in ws]
+        own.step(gs, ms, ws, lr=0.02, beta=0.95, ns_steps=ns_steps)
+        assert own.status() == dm.OK
+        for i, s in enumerate(shapes):
+            m_ref[i], o_ref, w_new = oracle.muon_step(
+                np64(gs[i]), m_ref[i], w_before[i], lr=0.02, beta=0.95, ns_steps=ns_steps,
+                variant="gram" if (variant == 1 and max(s) >= 2 * min(s)) else "standard")
+            assert rel(np64(ms[i]), m_ref[i]) <= 1e-5, f"momentum {s}"
+            dw = np64(ws[i]) - w_before[i]
+            err = rel(dw, w_new - w_before[i])
+            worst = max(worst, err)
+            assert err <= 2e-2 + (1e-2 if wdt == torch.bfloat16 else 0.0), \
+                f"step {step} {s}: dW rel err {err:.3e}"
+    return worst
+
+
+def test_muon_step_single_256x1024_fp32(dm, wl):
+    _muon_case(dm, wl, [(256, 1024)], torch.float32, torch.float32)
+
+
+def test_muon_step_mixed_projection_set(dm, wl):
+    shapes = [(256, 256), (64, 256), (64, 256), (256, 256), (700, 256), (700, 256), (256, 700)]
+    _muon_case(dm, wl, shapes, torch.bfloat16, torch.float32)
+
+
+def test_muon_step_gram_variant(dm, wl):
+    shapes = [(256, 256), (64, 256), (700, 256), (256, 700)]
+    _muon_case(dm, wl, shapes, torch.bfloat16, torch.float32, variant=1)
+
+
+# ------------------------------------------------------------------ failure path
+def test_bounded_wait_timeout_is_reported_and_context_survives(dm, wl):
+    ps = PackedSet(dm, [(64, 128)])
+    dm.debug_wait_timeout(ps.workspace, 2000)
+    assert dm.stream_status(ps.workspace) == dm.ERR_TIMEOUT
+    assert dm.stream_status(ps.workspace) == dm.OK     # cleared once read
+    u = wl.random_matrix((64, 128), 3, "cuda", 1.0, torch.bfloat16)
+    ps.view(0).copy_(u)
+    run_ns(dm, ps, 5)
+    assert rel(np64(ps.view(0)), oracle.newton_schulz(np64(u), 5)) <= 2e-2
