@@ -53,7 +53,7 @@ struct Plan {
   int sym_total = 0;
   size_t off_tables = 0, tables_bytes = 0;
   size_t off_ew = 0, off_bk = 0, off_imat = 0, off_sym = 0, off_tmaps = 0;
-  size_t off_partials = 0, off_inv = 0;
+  size_t off_partials = 0, off_inv = 0, off_shift = 0;
   size_t total = 0;
 };
 
@@ -165,7 +165,9 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
   P.off_partials = off;
   off = align_up(off + size_t(P.total_chunks) * sizeof(float), 256);
   P.off_inv = off;
-  off = align_up(off + size_t(n) * sizeof(float), 4096);
+  off = align_up(off + size_t(n) * sizeof(float), 256);
+  P.off_shift = off;
+  off = align_up(off + size_t(P.n_internal) * sizeof(float), 4096);
   for (auto& B : P.buckets) {
     for (int s = 0; s < kSlots; ++s) {
       if (!B.used[s]) continue;
@@ -415,21 +417,30 @@ struct GemmLauncher {
     return g;
   }
   // out = alpha*I + beta*aux + gamma*L R^T  (m x m, symmetric)
-  bool sym(int sL, int sR, int sAux, int sOut, float alpha, float beta, float gamma) const {
+  bool sym(int sL, int sR, int sAux, int sOut, float alpha, float beta, float gamma,
+           const float* shift = nullptr, float shift_sign = 0.f) const {
     GemmArgs g = base();
     g.total_tiles = sym_tiles;
     g.sL = sL; g.sR = sR; g.sAux = sAux; g.sOut = sOut;
     g.alpha = alpha; g.beta = beta; g.gamma = gamma;
+    g.shift = shift; g.shift_sign = shift_sign;
     return launch_ns_gemm(g, false, sms, R.stream) == cudaSuccess;
   }
   // out = alpha*aux + gamma*L R  (m x n); final: write O into the packed buffer
-  bool full(int sL, int sR, int sAux, int sOut, float alpha, float gamma, bool final) const {
+  bool full(int sL, int sR, int sAux, int sOut, float alpha, float gamma, bool final,
+            const float* shift = nullptr, float shift_sign = 0.f) const {
     GemmArgs g = base();
     g.total_tiles = full_tiles;
     g.sL = sL; g.sR = sR; g.sAux = sAux; g.sOut = sOut;
     g.alpha = alpha; g.beta = 0.f; g.gamma = gamma;
+    g.shift = shift; g.shift_sign = shift_sign;
     g.final_out = final ? 1 : 0;
     return launch_ns_gemm(g, true, sms, R.stream) == cudaSuccess;
+  }
+  int n_mats() const {
+    int k = 0;
+    for (int b = b0; b < b1; ++b) k += int(P.buckets[b].mats.size());
+    return k;
   }
 };
 
@@ -474,18 +485,27 @@ int run(const Request& R) {
       if (launch_relayout(ew, R.n, P.total_tiles, packed, inv, s) != cudaSuccess)
         return DMUON_ERR_CUDA;
       const float a = R.abc[0], b = R.abc[1], c = R.abc[2];
-      // standard buckets: per step A = X X^T; B = b A + c A A; X' = a X + B X
+      // standard buckets, per step:
+      //   A = X X^T;  d = b s + c s^2 with s = trace(A)/m;
+      //   B' = b A + c A A - d I;  X' = (a + d) X + B' X   (= a X + B X)
+      // Storing B' instead of B keeps B's large diagonal (about b + c once the
+      // singular values approach 1) out of the bf16 rounding, where it would be
+      // amplified by the cancellation between a X and B X.
       if (P.n_std > 0) {
         GemmLauncher L{P, R, D.sms, ws};
         L.b0 = 0;
         L.b1 = P.n_std;
         group_tiles(P, L.b0, L.b1, &L.sym_tiles, &L.full_tiles);
+        float* shift = reinterpret_cast<float*>(ws + P.off_shift);
+        const Bucket* bk = reinterpret_cast<const Bucket*>(ws + P.off_bk);
         for (int k = 0; k < R.ns_steps; ++k) {
           const int xin = (k & 1) ? SX1 : SX0, xout = (k & 1) ? SX0 : SX1;
           const bool last = k + 1 == R.ns_steps;
           if (!L.sym(xin, xin, SM0, SM0, 0.f, 0.f, 1.f)) return DMUON_ERR_CUDA;
-          if (!L.sym(SM0, SM0, SM0, SM1, 0.f, b, c)) return DMUON_ERR_CUDA;
-          if (!L.full(SM1, xin, xin, xout, a, 1.f, last)) return DMUON_ERR_CUDA;
+          if (launch_diag_shift(bk, P.n_std, 0, L.n_mats(), SM0, b, c, shift, s) != cudaSuccess)
+            return DMUON_ERR_CUDA;
+          if (!L.sym(SM0, SM0, SM0, SM1, 0.f, b, c, shift, -1.f)) return DMUON_ERR_CUDA;
+          if (!L.full(SM1, xin, xin, xout, a, 1.f, last, shift, 1.f)) return DMUON_ERR_CUDA;
         }
       }
       // Gram buckets: A0 = X0 X0^T; per step P = aI + bA + cA^2, Q = P Q,

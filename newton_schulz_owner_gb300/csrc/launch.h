@@ -11,6 +11,10 @@ namespace dm {
 size_t ns_gemm_smem_bytes();
 cudaError_t ns_gemm_prepare();  // once per device: opt into large shared memory
 cudaError_t launch_ns_gemm(const GemmArgs& g, bool full, int num_sms, cudaStream_t s);
+// Per-matrix diagonal shift b*s + c*s^2 with s = trace(A)/m, A = slot `slot`.
+cudaError_t launch_diag_shift(const Bucket* buckets, int n_buckets, int first_internal,
+                              int n_mats, int slot, float b, float c, float* shift,
+                              cudaStream_t s);
 
 // elementwise.cu
 // Copy `bytes` (multiple of 16) from host memory into device memory through

@@ -237,7 +237,7 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
 
 template <bool FULL>
 DM_DEV void store_tile_chunk(const GemmArgs& g, const Bucket& B, const TileInfo& T, int r,
-                             int c0, const float (&acc)[32]) {
+                             int c0, float alpha, const float (&acc)[32]) {
   float o[32];
   if (!FULL) {
     const int m = B.m;
@@ -252,11 +252,11 @@ DM_DEV void store_tile_chunk(const GemmArgs& g, const Bucket& B, const TileInfo&
 #pragma unroll
       for (int j = 0; j < 32; ++j) o[j] = g.gamma * acc[j];
     }
-    if (g.alpha != 0.f) {
+    if (alpha != 0.f) {
       const int d = r - c0;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (j == d) o[j] += g.alpha;
+        if (j == d) o[j] += alpha;
     }
     __nv_bfloat16* row = out + (long long)r * pm;
     if (c0 >= r && c0 + 32 <= m) {
@@ -276,12 +276,12 @@ DM_DEV void store_tile_chunk(const GemmArgs& g, const Bucket& B, const TileInfo&
     }
   } else {
     const int m = B.m, n = B.n;
-    if (g.alpha != 0.f) {
+    if (alpha != 0.f || g.shift != nullptr) {
       float x[32];
       load_bf16x32(B.slot[g.sAux] + (long long)T.mat * B.stride_x + (long long)r * B.pitch_x + c0,
                    x);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = fmaf(g.gamma, acc[j], g.alpha * x[j]);
+      for (int j = 0; j < 32; ++j) o[j] = fmaf(g.gamma, acc[j], alpha * x[j]);
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j) o[j] = g.gamma * acc[j];
@@ -340,6 +340,8 @@ DM_DEV void epilogue(const GemmArgs& g, uint64_t* tfull, uint64_t* tempty, uint3
     tc_fence_after();
     const int r = T.ti * kBM + q * 32 + lane;
     const int ncols = FULL ? B.n : B.m;
+    const float alpha =
+        g.shift != nullptr ? g.alpha + g.shift_sign * g.shift[B.first + T.mat] : g.alpha;
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {
       const int tcol = h * 128 + cc * 32;
@@ -348,7 +350,7 @@ DM_DEV void epilogue(const GemmArgs& g, uint64_t* tfull, uint64_t* tempty, uint3
       float v[32];
       tmem_ld32(tmem_base + uint32_t(acc * kAccCols + tcol) + (uint32_t(q * 32) << 16), v);
       tmem_ld_wait();
-      if (r < B.m) store_tile_chunk<FULL>(g, B, T, r, c0, v);
+      if (r < B.m) store_tile_chunk<FULL>(g, B, T, r, c0, alpha, v);
     }
     tc_fence_before();
     __syncwarp();
@@ -411,7 +413,49 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   }
 }
 
+// One block per matrix: s = trace(A) / m in a fixed order, then
+// shift = b*s + c*s^2, the value of b*A + c*A^2 on the diagonal when A is
+// close to s*I.  The polynomial launch subtracts it from the diagonal of B and
+// the axpy launch adds it to a, which leaves a*X + B*X unchanged in exact
+// arithmetic but keeps the large diagonal of B out of its bf16 rounding.
+__global__ void __launch_bounds__(256) diag_shift_kernel(const Bucket* __restrict__ buckets,
+                                                         int n_buckets, int first_internal,
+                                                         int slot, float b, float c,
+                                                         float* shift) {
+  __shared__ float red[256];
+  const int internal = first_internal + blockIdx.x;
+  int lo = 0, hi = n_buckets - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (buckets[mid].first <= internal) lo = mid;
+    else hi = mid - 1;
+  }
+  const Bucket& B = buckets[lo];
+  const int mat = internal - B.first;
+  const __nv_bfloat16* A = B.slot[slot] + (long long)mat * B.stride_m;
+  float s = 0.f;
+  for (int j = threadIdx.x; j < B.m; j += 256) s += __bfloat162float(A[(long long)j * B.pitch_m + j]);
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const float t = red[0] / float(B.m);
+    shift[internal] = fmaf(c * t, t, b * t);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_diag_shift(const Bucket* buckets, int n_buckets, int first_internal,
+                              int n_mats, int slot, float b, float c, float* shift,
+                              cudaStream_t s) {
+  if (n_mats <= 0) return cudaSuccess;
+  diag_shift_kernel<<<n_mats, 256, 0, s>>>(buckets, n_buckets, first_internal, slot, b, c, shift);
+  return cudaGetLastError();
+}
 
 size_t ns_gemm_smem_bytes() { return kSmemBytes; }
 

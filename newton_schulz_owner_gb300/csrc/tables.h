@@ -75,6 +75,8 @@ constexpr int kBM = 128, kBN = 256, kBK = 64;
 //     out = alpha * I + beta * aux + gamma * (L R^T)
 //   full product (m x n output):
 //     out = alpha * aux + gamma * (L R)        (L: m x m, R: m x n)
+// When `shift` is set, alpha becomes alpha + shift_sign * shift[matrix] per
+// matrix (internal order).
 struct GemmArgs {
   const Bucket* buckets;
   const unsigned char* tmaps;    // CUtensorMap array, 128 bytes each
@@ -85,8 +87,10 @@ struct GemmArgs {
   int n_buckets;
   int total_tiles;
   int sL, sR, sAux, sOut;
+  const float* shift;            // per-matrix diagonal shift, or null
   int final_out;                 // full product: write O into `packed`
   float alpha, beta, gamma;
+  float shift_sign;
 };
 
 }  // namespace dm
