@@ -351,7 +351,7 @@ def run_gpu(args, rank, world, local_rank):
                "d2h_bytes_per_step": int(d2h)}
         del G_host, W_host
 
-    launches_per_step = count_launches(lambda: step_phases())
+    launches_per_step = None if args.no_launch_count else count_launches(lambda: step_phases())
 
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
@@ -392,7 +392,7 @@ def run_gpu(args, rank, world, local_rank):
         "phases": phases,
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": None if launches_per_step is None else launches_per_step * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -417,6 +417,8 @@ def main():
     ap.add_argument("--impl", default="dmuon", choices=["dmuon", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-launch-count", action="store_true",
+                    help="skip the CUDA-profiler launch count (use under ncu)")
     args = ap.parse_args()
     rank, world, local_rank = _rank_env()
     if args.impl == "reference":

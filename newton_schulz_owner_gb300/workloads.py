@@ -68,6 +68,10 @@ WORKLOADS: Dict[str, Workload] = {
     "llama-3.2-3b": Workload("llama-3.2-3b", 2, 28, _layer(3072, 1024, 8192), n_owners=8),
     "llama-3.1-8b": Workload("llama-3.1-8b", 3, 32, _layer(4096, 1024, 14336)),
     "qwen2.5-7b": Workload("qwen2.5-7b", 4, 28, _layer(3584, 512, 18944)),
+    # One layer of the Llama-3.1-8B set (7 matrices, 218 M elements, ~3.5 GB on
+    # the device with workspace): the same kernels on a case small enough for
+    # multi-pass profiler captures.
+    "llama-3.1-8b-layer": Workload("llama-3.1-8b-layer", 5, 1, _layer(4096, 1024, 14336)),
 }
 
 
