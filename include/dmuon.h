@@ -179,6 +179,43 @@ int dmuon_stream_status(cudaStream_t stream, void* workspace);
 int dmuon_debug_wait_timeout(void* workspace, size_t ws_bytes, int budget_us,
                              cudaStream_t stream);
 
+/* Bytes of the library's built-in scratch array (see dmuon_ns_batched_noalloc). */
+#define DMUON_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * dmuon_ns_batched_noalloc -- dmuon_ns_batched without a caller workspace, for
+ * callers that cannot allocate device memory at all: code that runs where
+ * cudaMalloc is forbidden or would stall (inside a host framework that owns
+ * every device allocation, a plugin that may only use the buffers it is
+ * handed, a latency-critical loop where cudaMalloc's implicit device
+ * synchronisation is not acceptable).  The DMuon pages have no counterpart to
+ * this call; it is a convenience of this library.
+ *
+ * Scratch comes from one file-scope __device__ array of
+ * DMUON_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library.  Every GPU that
+ * loads the library holds that array until the process exits.  The call
+ * allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ * The caller still passes the packed input/output buffer and the offsets,
+ * with the same meaning and layout as for dmuon_ns_batched; the norms are taken
+ * from the bf16 packed values (use_pack_norms = 0).
+ *
+ *  - Set-up: the first call on a device (with that device current) looks up
+ *    the array's device address once and keeps it; make that first call
+ *    before any stream capture.
+ *  - Size limit: a shape list whose dmuon_workspace_bytes exceeds
+ *    DMUON_NOALLOC_SCRATCH_BYTES is rejected with DMUON_ERR_WORKSPACE before
+ *    anything is enqueued (e.g. 1024 x 4096 fits, 4096 x 4096 does not).
+ *  - Sharing: every call on a device uses the same array, which keeps the last
+ *    call's contents.  Calls whose work overlaps on the GPU (two streams, two
+ *    host threads without ordering) race on it and give wrong results; order
+ *    them on one stream.  Each call clears the array's device error word when
+ *    it starts; a bounded wait that gives up inside this call leaves the
+ *    outputs incomplete and is not reported to the caller.
+ */
+int dmuon_ns_batched_noalloc(int n, const dmuon_shape* shp, void* packed_bf16,
+                             const int64_t* offset, int ns_steps, int ns_variant,
+                             const float* abc, float eps, cudaStream_t stream);
+
 /* Human-readable text for a status code (static storage). */
 const char* dmuon_status_string(int status);
 

@@ -547,9 +547,63 @@ int run(const Request& R) {
 }  // namespace
 }  // namespace dm
 
+// Built-in scratch of dmuon_ns_batched_noalloc.  Host code may not use the
+// array's name as an address: the device address comes from
+// cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DMUON_NOALLOC_SCRATCH_BYTES];
+
+namespace dm {
+namespace {
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (null on error).
+void* noalloc_scratch() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_noalloc_ptr[d] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    g_noalloc_ptr[d] = p;
+  }
+  return g_noalloc_ptr[d];
+}
+}  // namespace
+}  // namespace dm
+
 using namespace dm;
 
 extern "C" {
+
+int dmuon_ns_batched_noalloc(int n, const dmuon_shape* shp, void* packed_bf16,
+                             const int64_t* offset, int ns_steps, int ns_variant,
+                             const float* abc, float eps, cudaStream_t stream) {
+  Request R;
+  R.n = n; R.shp = shp; R.packed = packed_bf16; R.offset = offset; R.ns_steps = ns_steps;
+  R.variant = ns_variant;
+  if (abc != nullptr) { R.abc[0] = abc[0]; R.abc[1] = abc[1]; R.abc[2] = abc[2]; }
+  R.eps = eps; R.pack_norms = false; R.stream = stream; R.do_ns = true;
+  // host-side checks first: nothing is enqueued for a rejected call
+  if (n < 0 || (n > 0 && shp == nullptr)) return DMUON_ERR_INVALID_ARG;
+  Plan P;
+  int st = build_plan(n, shp, ns_variant, P);
+  if (st != DMUON_OK) return st;
+  if (P.total > size_t(DMUON_NOALLOC_SCRATCH_BYTES)) return DMUON_ERR_WORKSPACE;
+  if (n == 0) return DMUON_OK;
+  DevInfo D;
+  st = device_info(&D);
+  if (st != DMUON_OK) return st;
+  void* scratch = noalloc_scratch();
+  if (scratch == nullptr) return DMUON_ERR_CUDA;
+  R.ws = scratch;
+  R.ws_bytes = DMUON_NOALLOC_SCRATCH_BYTES;
+  st = check_request(R, P);
+  if (st != DMUON_OK) return st;
+  // the device error word must start at zero; everything else in the scratch
+  // is written before it is read
+  if (cudaMemsetAsync(scratch, 0, sizeof(int), stream) != cudaSuccess) return DMUON_ERR_CUDA;
+  return run(R);
+}
 
 int dmuon_plan(int n, const dmuon_shape* shp, int n_owners, int* owner_of, int64_t* offset,
                int64_t* owner_elems) {

@@ -28,7 +28,9 @@ DEFAULT_ABC = (3.4445, -4.7750, 2.0315)
 
 EXPORTED = ("dmuon_plan", "dmuon_workspace_bytes", "dmuon_pack", "dmuon_ns_batched",
             "dmuon_unpack_update", "dmuon_muon_step", "dmuon_stream_status",
-            "dmuon_debug_wait_timeout", "dmuon_status_string", "dmuon_version")
+            "dmuon_debug_wait_timeout", "dmuon_ns_batched_noalloc", "dmuon_status_string",
+            "dmuon_version")
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class Shape(ctypes.Structure):
@@ -54,6 +56,9 @@ _lib.dmuon_unpack_update.restype = _i
 _lib.dmuon_muon_step.argtypes = [_i, _ShapeP, _VPP, _i, _VPP, _VPP, _i, _f, _f, _i, _i, _vp,
                                  _i64p, _vp, _sz, _vp]
 _lib.dmuon_muon_step.restype = _i
+_lib.dmuon_ns_batched_noalloc.argtypes = [_i, _ShapeP, _vp, _i64p, _i, _i,
+                                          ctypes.POINTER(ctypes.c_float), _f, _vp]
+_lib.dmuon_ns_batched_noalloc.restype = _i
 _lib.dmuon_stream_status.argtypes = [_vp, _vp]
 _lib.dmuon_stream_status.restype = _i
 _lib.dmuon_debug_wait_timeout.argtypes = [_vp, _sz, _i, _vp]
@@ -164,6 +169,18 @@ def ns_batched(shapes, packed, offsets, workspace, ns_steps: int = 5, variant: i
     _check(_lib.dmuon_ns_batched(n, _shapes(shapes), _addr(packed), _i64(offsets), int(ns_steps),
                                  int(variant), abc_arr, float(eps), int(bool(use_pack_norms)),
                                  _addr(workspace), wsb, _stream(stream)), "dmuon_ns_batched")
+
+
+def ns_batched_noalloc(shapes, packed, offsets, ns_steps: int = 5, variant: int = NS_STANDARD,
+                       abc: Optional[Sequence[float]] = None, eps: float = 1e-7,
+                       stream=None) -> None:
+    """dmuon_ns_batched on the library's built-in scratch array (no workspace,
+    no device allocation); problems up to NOALLOC_SCRATCH_BYTES of workspace."""
+    abc_arr = None if abc is None else (ctypes.c_float * 3)(*[float(v) for v in abc])
+    _check(_lib.dmuon_ns_batched_noalloc(len(shapes), _shapes(shapes), _addr(packed),
+                                         _i64(offsets), int(ns_steps), int(variant), abc_arr,
+                                         float(eps), _stream(stream)),
+           "dmuon_ns_batched_noalloc")
 
 
 def unpack_update(shapes, weights, lr, packed, offsets, workspace, stream=None) -> None:
