@@ -138,11 +138,12 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
       B.used[SX0] = true;
       for (int s = SM0; s <= SM5; ++s) B.used[s] = true;
     }
-    const int I = int(ceil_div(B.m, kBM)), J = int(ceil_div(B.m, kBN));
-    for (int ti = 0; ti < I; ++ti)
-      for (int tj = (ti * kBM) / kBN; tj < J; ++tj) B.sym.push_back((ti << 16) | tj);
-    B.full_ti = I;
-    B.full_tj = int(ceil_div(B.n, kBN));
+    // upper-triangle 256 x 256 tiles (diagonal tiles included) of an m x m product
+    const int J = int(ceil_div(B.m, kTileM));
+    for (int ti = 0; ti < J; ++ti)
+      for (int tj = ti; tj < J; ++tj) B.sym.push_back((ti << 16) | tj);
+    B.full_ti = J;
+    B.full_tj = int(ceil_div(B.n, kTileN));
     P.sym_total += int(B.sym.size());
   }
   P.n_internal = internal;
@@ -186,6 +187,7 @@ struct DevInfo {
   int status = DMUON_OK;
   int sms = 0;
   int clock_khz = 0;
+  int max_clusters = 0;  // resident CTA pairs of the product kernel
 };
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
@@ -205,7 +207,7 @@ int device_info(DevInfo* out) {
       return DMUON_ERR_CUDA;
     if (major != 10 || minor != 3) {
       D.status = DMUON_ERR_UNSUPPORTED;
-    } else if (ns_gemm_prepare() != cudaSuccess) {
+    } else if (ns_gemm_prepare(D.sms, &D.max_clusters) != cudaSuccess) {
       return DMUON_ERR_CUDA;
     }
     D.ready = true;
@@ -401,7 +403,7 @@ void group_tiles(const Plan& P, int b0, int b1, int* sym_tiles, int* full_tiles)
 struct GemmLauncher {
   const Plan& P;
   const Request& R;
-  int sms;
+  int clusters;
   unsigned char* ws;
   int b0 = 0, b1 = 0, sym_tiles = 0, full_tiles = 0;
 
@@ -424,7 +426,7 @@ struct GemmLauncher {
     g.sL = sL; g.sR = sR; g.sAux = sAux; g.sOut = sOut;
     g.alpha = alpha; g.beta = beta; g.gamma = gamma;
     g.shift = shift; g.shift_sign = shift_sign;
-    return launch_ns_gemm(g, false, sms, R.stream) == cudaSuccess;
+    return launch_ns_gemm(g, false, clusters, R.stream) == cudaSuccess;
   }
   // out = alpha*aux + gamma*L R  (m x n); final: write O into the packed buffer
   bool full(int sL, int sR, int sAux, int sOut, float alpha, float gamma, bool final,
@@ -435,7 +437,7 @@ struct GemmLauncher {
     g.alpha = alpha; g.beta = 0.f; g.gamma = gamma;
     g.shift = shift; g.shift_sign = shift_sign;
     g.final_out = final ? 1 : 0;
-    return launch_ns_gemm(g, true, sms, R.stream) == cudaSuccess;
+    return launch_ns_gemm(g, true, clusters, R.stream) == cudaSuccess;
   }
   int n_mats() const {
     int k = 0;
@@ -492,7 +494,7 @@ int run(const Request& R) {
       // singular values approach 1) out of the bf16 rounding, where it would be
       // amplified by the cancellation between a X and B X.
       if (P.n_std > 0) {
-        GemmLauncher L{P, R, D.sms, ws};
+        GemmLauncher L{P, R, D.max_clusters, ws};
         L.b0 = 0;
         L.b1 = P.n_std;
         group_tiles(P, L.b0, L.b1, &L.sym_tiles, &L.full_tiles);
@@ -512,7 +514,7 @@ int run(const Request& R) {
       // A' = A P^2; finally O = Q X0.  Slots: A in SM0/SM1, P in SM2 (SM3 at
       // step 0, where Q = P), Q in SM3/SM4, T = P^2 in SM5.
       if (P.n_std < int(P.buckets.size())) {
-        GemmLauncher L{P, R, D.sms, ws};
+        GemmLauncher L{P, R, D.max_clusters, ws};
         L.b0 = P.n_std;
         L.b1 = int(P.buckets.size());
         group_tiles(P, L.b0, L.b1, &L.sym_tiles, &L.full_tiles);

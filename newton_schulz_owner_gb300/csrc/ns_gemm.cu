@@ -10,14 +10,23 @@
 // The standard Muon iteration is these three launches per step; the Gram
 // variant chains symmetric launches on m x m matrices.
 //
+// Work unit: a 256 x 256 output tile computed by a cluster of two CTAs on two
+// SMs with one tcgen05.mma.cta_group::2 (M=256, N=256, K=16).  Each CTA loads
+// only its 128 rows of L and its 128 columns of R per 64-wide K block (32 KB),
+// half of what a single SM needs for a 128 x 256 tile at the same tensor
+// rate, which leaves room for a 6-stage ring in 192 KB of shared memory.
+//
 // CTA layout (320 threads, one CTA per SM, persistent over tiles):
-//   warp 0      TMA producer: 128x64 tile of L and 256x64 tile of R per stage,
-//               128-byte swizzle, 4-stage ring of shared memory
-//   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
-//               (M=128, N=256, K=16) into one of two 256-column accumulators
-//   warps 2-9   epilogue: tcgen05.ld, fused polynomial / axpy, bf16 stores
-// Tiles are handed out statically (tile = blockIdx.x + k * gridDim.x), so each
-// role walks the same sequence without talking to the others.
+//   warp 0      TMA producer (both CTAs): completion counted on the leader's
+//               (rank 0) barrier
+//   warp 1      allocates 512 TMEM columns (two 256-column accumulators) for
+//               the pair; in the leader, lane 0 issues the MMAs and commits
+//               to the barriers of both CTAs
+//   warps 2-9   epilogue (both CTAs): tcgen05.ld of this CTA's 128 rows, fused
+//               polynomial / axpy, bf16 stores, then release the accumulator
+//               to the leader
+// Pair tiles are handed out statically (tile = cluster + k * clusters), so all
+// roles of both CTAs walk the same sequence without talking to each other.
 #include "dmuon.h"
 #include "launch.h"
 #include "ptx.cuh"
@@ -28,17 +37,21 @@
 namespace dm {
 namespace {
 
-constexpr int kStages = 4;
-constexpr int kAStage = kBM * kBK * 2;  // 16 KB
-constexpr int kBStage = kBN * kBK * 2;  // 32 KB
+constexpr int kStages = 6;
+constexpr int kAStage = kCtaM * kBK * 2;         // 16 KB: this CTA's 128 rows of L
+constexpr int kBStage = (kTileN / 2) * kBK * 2;  // 16 KB: this CTA's 128 columns of R
 constexpr int kStageBytes = kAStage + kBStage;
-constexpr int kBox = 64 * 64 * 2;       // one TMA box: 64 rows x 128 bytes
+constexpr int kPairTxBytes = 2 * kStageBytes;    // both CTAs' loads land on the leader's barrier
+constexpr int kBox = 64 * 64 * 2;                // one TMA box: 64 rows x 128 bytes
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
 constexpr int kBarBytes = 256;
 constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 + kBarBytes;
+// After a bounded wait gives up, wait this long before leaving so that copies
+// and MMAs already issued to this CTA's shared memory / TMEM have landed.
+constexpr long long kAbortSettleCycles = 400000;
 
 struct TileInfo {
   int bucket, mat, ti, tj;
@@ -126,13 +139,14 @@ DM_DEV void store_bf16x32(__nv_bfloat16* p, const float (&f)[32]) {
 
 // ------------------------------------------------------------------ roles
 template <bool FULL>
-DM_DEV void producer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* full_bar,
-                     uint64_t* empty_bar, volatile int* abort_flag) {
+DM_DEV void producer(const GemmArgs& g, uint32_t rank, uint8_t* sA, uint8_t* sB,
+                     uint64_t* full_bar, uint64_t* empty_bar, volatile int* abort_flag) {
+  const uint32_t leader_full = mapa_shared(smem_u32(full_bar), 0);
+  const int clusters = int(cluster_count_x());
   int stage = 0;
   uint32_t phase = 0;
-  uint32_t issued = 0, last_parity = 0;
   int prev_bucket = -1;
-  for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x) {
+  for (int t = int(cluster_id_x()); t < g.total_tiles; t += clusters) {
     const TileInfo T = decode_tile<FULL>(g, t);
     const Bucket& B = g.buckets[T.bucket];
     const void* mapL = tmap_of(g, B, g.sL);
@@ -143,58 +157,52 @@ DM_DEV void producer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* full
       prev_bucket = T.bucket;
     }
     const int KB = (k_extent<FULL>(g, B) + kBK - 1) / kBK;
-    const int row0 = T.ti * kBM;
-    const int col0 = T.tj * kBN;
+    const int row0 = T.ti * kTileM + int(rank) * kCtaM;        // this CTA's rows of L
+    const int col0 = T.tj * kTileN + int(rank) * (kTileN / 2);  // this CTA's columns of R
     for (int kb = 0; kb < KB; ++kb) {
       if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
         raise_abort(g.err, abort_flag);
-        goto drain;
+        return;
       }
-      mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
-      {
-        uint8_t* a = sA + stage * kAStage;
-        uint8_t* b = sB + stage * kBStage;
-        const int k0 = kb * kBK;
-        tma_load_3d(a, mapL, &full_bar[stage], k0, row0, T.mat);
-        tma_load_3d(a + kBox, mapL, &full_bar[stage], k0, row0 + 64, T.mat);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (FULL)  // R = X, MN-major: 64 K-rows x 64 columns per box
-            tma_load_3d(b + q * kBox, mapR, &full_bar[stage], col0 + 64 * q, k0, T.mat);
-          else       // R rows, K-major
-            tma_load_3d(b + q * kBox, mapR, &full_bar[stage], k0, col0 + 64 * q, T.mat);
-        }
+      if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], kPairTxBytes);
+      uint8_t* a = sA + stage * kAStage;
+      uint8_t* b = sB + stage * kBStage;
+      const uint32_t bar = leader_full + uint32_t(stage) * 8u;
+      const int k0 = kb * kBK;
+      tma_load_3d_pair(a, mapL, bar, k0, row0, T.mat);
+      tma_load_3d_pair(a + kBox, mapL, bar, k0, row0 + 64, T.mat);
+      if (FULL) {  // R = X, MN-major: 64 K-rows x 64 columns per box
+        tma_load_3d_pair(b, mapR, bar, col0, k0, T.mat);
+        tma_load_3d_pair(b + kBox, mapR, bar, col0 + 64, k0, T.mat);
+      } else {     // R rows, K-major
+        tma_load_3d_pair(b, mapR, bar, k0, col0, T.mat);
+        tma_load_3d_pair(b + kBox, mapR, bar, k0, col0 + 64, T.mat);
       }
-      issued |= 1u << stage;
-      last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
   }
-drain:
-  // Never leave with bulk copies still landing in shared memory.
-  for (int s = 0; s < kStages; ++s)
-    if (issued & (1u << s)) (void)mbar_wait(&full_bar[s], (last_parity >> s) & 1u, nullptr);
 }
 
 template <bool FULL>
 DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* full_bar,
                        uint64_t* empty_bar, uint64_t* tfull, uint64_t* tempty,
                        uint64_t* drain_bar, uint32_t tmem_base, volatile int* abort_flag) {
-  constexpr uint32_t idesc = idesc_bf16(kBM, kBN, FULL);
+  constexpr uint32_t idesc = idesc_bf16(kTileM, kTileN, FULL);
   const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+  const int clusters = int(cluster_count_x());
   int stage = 0;
   uint32_t phase = 0;
   int it = 0;
-  for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x, ++it) {
+  for (int t = int(cluster_id_x()); t < g.total_tiles; t += clusters, ++it) {
     const TileInfo T = decode_tile<FULL>(g, t);
     const Bucket& B = g.buckets[T.bucket];
     const int KB = (k_extent<FULL>(g, B) + kBK - 1) / kBK;
     const int acc = it & 1;
     const uint32_t aph = uint32_t(it >> 1) & 1u;
-    if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag)) {
+    if (!mbar_wait_cluster(&tempty[acc], aph ^ 1u, abort_flag)) {
       raise_abort(g.err, abort_flag);
       break;
     }
@@ -202,7 +210,7 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
     const uint32_t d = tmem_base + uint32_t(acc * kAccCols);
     bool ok = true;
     for (int kb = 0; kb < KB; ++kb) {
-      if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+      if (!mbar_wait_cluster(&full_bar[stage], phase, abort_flag)) {
         raise_abort(g.err, abort_flag);
         ok = false;
         break;
@@ -219,19 +227,19 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
         // apart (SBO); 16 K-rows = 2 KB.  K-major R as for L.
         const uint64_t bd = FULL ? sdesc_sw128(sb + uint32_t(k * 2048), kBox, 1024)
                                  : sdesc_sw128(sb + uint32_t(k * 32), 16, 1024);
-        umma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+        umma_bf16_pair(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
       }
-      umma_commit(&empty_bar[stage]);
+      umma_commit_pair(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
     if (!ok) break;
-    umma_commit(&tfull[acc]);
+    umma_commit_pair(&tfull[acc], 0x3);  // accumulator ready in both CTAs
   }
   // Every issued MMA must finish before TMEM and shared memory go away.
-  umma_commit(drain_bar);
+  umma_commit_pair(drain_bar, 0x1);
   (void)mbar_wait(drain_bar, 0, nullptr);
 }
 
@@ -319,33 +327,35 @@ DM_DEV void store_tile_chunk(const GemmArgs& g, const Bucket& B, const TileInfo&
 }
 
 template <bool FULL>
-DM_DEV void epilogue(const GemmArgs& g, uint64_t* tfull, uint64_t* tempty, uint32_t tmem_base,
-                     volatile int* abort_flag) {
+DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t* tempty,
+                     uint32_t tmem_base, volatile int* abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;          // TMEM lane quarter this warp may read
   const int h = (warp - 2) >> 2;   // which 128-column half of the tile
+  const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
+  const int clusters = int(cluster_count_x());
   int it = 0;
-  for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x, ++it) {
+  for (int t = int(cluster_id_x()); t < g.total_tiles; t += clusters, ++it) {
     const TileInfo T = decode_tile<FULL>(g, t);
     const Bucket& B = g.buckets[T.bucket];
     const int acc = it & 1;
     const uint32_t aph = uint32_t(it >> 1) & 1u;
     int ok = 1;
-    if (lane == 0) ok = mbar_wait(&tfull[acc], aph, abort_flag) ? 1 : 0;
+    if (lane == 0) ok = mbar_wait_cluster(&tfull[acc], aph, abort_flag) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) {
       if (lane == 0) raise_abort(g.err, abort_flag);
       break;
     }
     tc_fence_after();
-    const int r = T.ti * kBM + q * 32 + lane;
+    const int r = T.ti * kTileM + int(rank) * kCtaM + q * 32 + lane;
     const int ncols = FULL ? B.n : B.m;
     const float alpha =
         g.shift != nullptr ? g.alpha + g.shift_sign * g.shift[B.first + T.mat] : g.alpha;
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {
       const int tcol = h * 128 + cc * 32;
-      const int c0 = T.tj * kBN + tcol;
+      const int c0 = T.tj * kTileN + tcol;
       if (c0 >= ncols) break;  // warp-uniform
       float v[32];
       tmem_ld32(tmem_base + uint32_t(acc * kAccCols + tcol) + (uint32_t(q * 32) << 16), v);
@@ -354,7 +364,7 @@ DM_DEV void epilogue(const GemmArgs& g, uint64_t* tfull, uint64_t* tempty, uint3
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&tempty[acc]);
+    if (lane == 0) mbar_arrive_cluster(leader_tempty + uint32_t(acc) * 8u);
   }
 }
 
@@ -374,42 +384,50 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
+  const uint32_t rank = cluster_rank();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&full_bar[s], 1);    // leader: its expect_tx; both CTAs' copies add bytes
+      mbar_init(&empty_bar[s], 1);   // the leader's commit
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps);
+      mbar_init(&tfull[a], 1);               // the leader's commit
+      mbar_init(&tempty[a], 2 * kEpiWarps);  // leader: every epilogue warp of both CTAs
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (threadIdx.x == 0) {
-    producer<FULL>(g, sA, sB, full_bar, empty_bar, abort_flag);
+    producer<FULL>(g, rank, sA, sB, full_bar, empty_bar, abort_flag);
   } else if (threadIdx.x == 32) {
-    mma_issuer<FULL>(g, sA, sB, full_bar, empty_bar, tfull, tempty, drain_bar, tmem_base,
-                     abort_flag);
+    if (rank == 0)
+      mma_issuer<FULL>(g, sA, sB, full_bar, empty_bar, tfull, tempty, drain_bar, tmem_base,
+                       abort_flag);
   } else if (warp >= 2) {
-    epilogue<FULL>(g, tfull, tempty, tmem_base, abort_flag);
+    epilogue<FULL>(g, rank, tfull, tempty, tmem_base, abort_flag);
   }
 
-  tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag != 0) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < kAbortSettleCycles) {
+    }
+  }
+  tc_fence_before();
+  cluster_sync();  // neither CTA leaves while the other may still touch its memory
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -447,6 +465,21 @@ __global__ void __launch_bounds__(256) diag_shift_kernel(const Bucket* __restric
   }
 }
 
+cudaLaunchConfig_t pair_config(int clusters, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned(2 * clusters), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  attr->id = cudaLaunchAttributeClusterDimension;
+  attr->val.clusterDim.x = 2;
+  attr->val.clusterDim.y = 1;
+  attr->val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 }  // namespace
 
 cudaError_t launch_diag_shift(const Bucket* buckets, int n_buckets, int first_internal,
@@ -459,23 +492,33 @@ cudaError_t launch_diag_shift(const Bucket* buckets, int n_buckets, int first_in
 
 size_t ns_gemm_smem_bytes() { return kSmemBytes; }
 
-cudaError_t ns_gemm_prepare() {
+cudaError_t ns_gemm_prepare(int num_sms, int* max_clusters) {
   cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(kSmemBytes));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(ns_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(kSmemBytes));
+  e = cudaFuncSetAttribute(ns_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr;
+  cudaLaunchConfig_t cfg = pair_config(num_sms / 2, nullptr, &attr);
+  int n0 = 0, n1 = 0;
+  e = cudaOccupancyMaxActiveClusters(&n0, ns_gemm_kernel<false>, &cfg);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveClusters(&n1, ns_gemm_kernel<true>, &cfg);
+  if (e != cudaSuccess) return e;
+  *max_clusters = n0 < n1 ? n0 : n1;
+  if (*max_clusters < 1) return cudaErrorInvalidConfiguration;
+  return cudaSuccess;
 }
 
-cudaError_t launch_ns_gemm(const GemmArgs& g, bool full, int num_sms, cudaStream_t s) {
+cudaError_t launch_ns_gemm(const GemmArgs& g, bool full, int max_clusters, cudaStream_t s) {
   if (g.total_tiles <= 0 || g.n_buckets <= 0) return cudaSuccess;
-  const int grid = g.total_tiles < num_sms ? g.total_tiles : num_sms;
-  if (full)
-    ns_gemm_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(g);
-  else
-    ns_gemm_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(g);
-  return cudaGetLastError();
+  const int clusters = g.total_tiles < max_clusters ? g.total_tiles : max_clusters;
+  cudaLaunchAttribute attr;
+  cudaLaunchConfig_t cfg = pair_config(clusters, s, &attr);
+  if (full) return cudaLaunchKernelEx(&cfg, ns_gemm_kernel<true>, g);
+  return cudaLaunchKernelEx(&cfg, ns_gemm_kernel<false>, g);
 }
 
 }  // namespace dm

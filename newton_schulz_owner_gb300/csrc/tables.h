@@ -67,8 +67,9 @@ struct InternalMat {
   int transposed;
 };
 
-// Tile shape of the Newton-Schulz products.
-constexpr int kBM = 128, kBN = 256, kBK = 64;
+// Tile shape of the Newton-Schulz products: a CTA pair computes a 256 x 256
+// tile; each CTA holds 128 of its rows (and loads half of its columns' operand).
+constexpr int kTileM = 256, kTileN = 256, kCtaM = 128, kBK = 64;
 
 // Launch arguments of the grouped Newton-Schulz product kernel.
 //   symmetric product (m x m output, upper-triangle tiles, mirrored):
