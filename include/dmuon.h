@@ -28,7 +28,8 @@
  *    shape / offset arrays are HOST arrays, read during the call only.
  *  - The library allocates no memory.  All scratch lives in the caller's
  *    `workspace` (size from dmuon_workspace_bytes, 256-byte aligned); the
- *    library copies its tables there with cudaMemcpyAsync on `stream`.
+ *    library writes its tables there with a small kernel on `stream` whose
+ *    parameters carry the bytes (no host staging buffer, no pageable copy).
  *  - Calls are asynchronous on `stream`.  Arguments are checked on the host
  *    before anything is enqueued; a bad argument returns an error and
  *    launches nothing.  Device-side failures (a bounded wait that gave up)
@@ -99,6 +100,9 @@ int dmuon_plan(int n, const dmuon_shape* shp, int n_owners, int* owner_of,
 /*
  * dmuon_workspace_bytes -- scratch bytes that dmuon_pack / dmuon_ns_batched /
  * dmuon_unpack_update / dmuon_muon_step need for this shape list and variant.
+ * dmuon_pack and dmuon_unpack_update use only the leading part of it (tables
+ * and norm partial sums), which is laid out the same for both variants, so one
+ * workspace sized for the variant in use serves all four calls.
  * Returns 0 for invalid arguments.  Touches no GPU.
  */
 size_t dmuon_workspace_bytes(int n, const dmuon_shape* shp, int ns_variant);
@@ -162,6 +166,36 @@ int dmuon_muon_step(int n, const dmuon_shape* shp, const void* const* grad, int 
                     size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * dmuon_adamw -- AdamW step for the parameters Muon does not own (home page,
+ * "LLM Pretraining": dmuon.Muon(..., adamw_lr=1e-3); "VLA and VLM":
+ * embeddings, norms and heads stay outside the Muon set).  The pages give only
+ * the learning rate; the update is the usual AdamW with decoupled weight decay:
+ *   p <- p * (1 - lr*wd)
+ *   m <- beta1*m + (1-beta1)*g;   v <- beta2*v + (1-beta2)*g^2
+ *   p <- p - lr/(1-beta1^t) * m / (sqrt(v)/sqrt(1-beta2^t) + eps)
+ * fp32 arithmetic; the hyper-parameters arrive in double and the per-step
+ * scalars (1-beta1, 1-beta2, the bias corrections, 1-lr*wd) are formed in
+ * double on the host and rounded to fp32 once.  A bf16 p is rounded to
+ * nearest even.  Typical values: beta1 0.9, beta2 0.999, eps 1e-8,
+ * weight_decay 0.01.
+ *   n            number of tensors (0 is a no-op)
+ *   numel[n]     host: elements of each tensor (any shape, contiguous)
+ *   param[n]     device, dtype param_dt (F32 or BF16), updated in place
+ *   grad[n]      device, dtype grad_dt (F32 or BF16)
+ *   exp_avg[n], exp_avg_sq[n]   device, fp32, updated in place
+ *   step         1-based step number t
+ *   workspace    device, 256-byte aligned, >= dmuon_adamw_workspace_bytes(n)
+ * One kernel launch for all tensors; 16-byte vector access where all four
+ * pointers of a tensor are 16-byte aligned.
+ */
+size_t dmuon_adamw_workspace_bytes(int n);
+int dmuon_adamw(int n, const int64_t* numel, void* const* param, int param_dt,
+                const void* const* grad, int grad_dt, float* const* exp_avg,
+                float* const* exp_avg_sq, double lr, double beta1, double beta2, double eps,
+                double weight_decay, int step, void* workspace, size_t ws_bytes,
+                cudaStream_t stream);
+
+/*
  * dmuon_stream_status -- synchronises `stream`, then reports (and clears) the
  * device error word kept in `workspace`: DMUON_OK, DMUON_ERR_TIMEOUT when a
  * bounded device wait gave up, DMUON_ERR_CUDA when the stream holds a CUDA
@@ -221,6 +255,13 @@ const char* dmuon_status_string(int status);
 
 /* Library version: major*10000 + minor*100 + patch. */
 int dmuon_version(void);
+
+/*
+ * dmuon_launch_count -- number of kernels the library has launched from the
+ * calling host thread (every call above counts its own launches) since the
+ * last reset; reset != 0 clears the count after reading it.
+ */
+long long dmuon_launch_count(int reset);
 
 #ifdef __cplusplus
 }

@@ -54,6 +54,7 @@ struct Plan {
   size_t off_tables = 0, tables_bytes = 0;
   size_t off_ew = 0, off_bk = 0, off_imat = 0, off_sym = 0, off_tmaps = 0;
   size_t off_partials = 0, off_inv = 0, off_shift = 0;
+  size_t prefix = 0;  // header, tables, norms: all that pack / update use; same for both variants
   size_t total = 0;
 };
 
@@ -169,6 +170,7 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
   off = align_up(off + size_t(n) * sizeof(float), 256);
   P.off_shift = off;
   off = align_up(off + size_t(P.n_internal) * sizeof(float), 4096);
+  P.prefix = off;
   for (auto& B : P.buckets) {
     for (int s = 0; s < kSlots; ++s) {
       if (!B.used[s]) continue;
@@ -272,7 +274,9 @@ struct Request {
 int check_request(const Request& R, const Plan& P) {
   if (R.packed == nullptr || R.ws == nullptr || R.offset == nullptr) return DMUON_ERR_INVALID_ARG;
   if (!aligned(R.packed, 256) || !aligned(R.ws, 256)) return DMUON_ERR_ALIGNMENT;
-  if (R.ws_bytes < P.total) return DMUON_ERR_WORKSPACE;
+  // pack and update never touch the Newton-Schulz buffers; their part of the
+  // layout does not depend on the variant
+  if (R.ws_bytes < (R.do_ns ? P.total : P.prefix)) return DMUON_ERR_WORKSPACE;
   if (R.do_pack) {
     if (R.grad == nullptr || R.momentum == nullptr) return DMUON_ERR_INVALID_ARG;
     if (R.grad_dt != DMUON_F32 && R.grad_dt != DMUON_BF16) return DMUON_ERR_INVALID_ARG;
@@ -364,7 +368,7 @@ int upload_tables(const Request& R, const Plan& P) {
     B.stride_m = BP.stride_m;
     B.tmap = int(b) * kSlots;
     for (int s = 0; s < kSlots; ++s) {
-      if (!BP.used[s]) continue;
+      if (!BP.used[s] || !R.do_ns) continue;
       void* base = ws + BP.slot_off[s];
       B.slot[s] = static_cast<__nv_bfloat16*>(base);
       const bool x = slot_is_x(s);
@@ -549,6 +553,13 @@ int run(const Request& R) {
 }  // namespace
 }  // namespace dm
 
+namespace dm {
+namespace {
+thread_local long long t_launches = 0;
+}  // namespace
+void note_launch(int kernels) { t_launches += kernels; }
+}  // namespace dm
+
 // Built-in scratch of dmuon_ns_batched_noalloc.  Host code may not use the
 // array's name as an address: the device address comes from
 // cudaGetSymbolAddress, once per device.
@@ -699,6 +710,75 @@ int dmuon_muon_step(int n, const dmuon_shape* shp, const void* const* grad, int 
   return run(R);
 }
 
+size_t dmuon_adamw_workspace_bytes(int n) {
+  if (n < 0) return 0;
+  return align_up(kHdrBytes + size_t(n) * sizeof(AdamTensor), 256);
+}
+
+int dmuon_adamw(int n, const int64_t* numel, void* const* param, int param_dt,
+                const void* const* grad, int grad_dt, float* const* exp_avg,
+                float* const* exp_avg_sq, double lr, double beta1, double beta2, double eps,
+                double weight_decay, int step, void* workspace, size_t ws_bytes,
+                cudaStream_t stream) {
+  if (n < 0) return DMUON_ERR_INVALID_ARG;
+  if (n == 0) return DMUON_OK;
+  if (numel == nullptr || param == nullptr || grad == nullptr || exp_avg == nullptr ||
+      exp_avg_sq == nullptr || workspace == nullptr)
+    return DMUON_ERR_INVALID_ARG;
+  if ((param_dt != DMUON_F32 && param_dt != DMUON_BF16) ||
+      (grad_dt != DMUON_F32 && grad_dt != DMUON_BF16))
+    return DMUON_ERR_INVALID_ARG;
+  if (step < 1 || !std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(weight_decay) ||
+      !(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0) || !(eps >= 0.0))
+    return DMUON_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return DMUON_ERR_ALIGNMENT;
+  if (ws_bytes < dmuon_adamw_workspace_bytes(n)) return DMUON_ERR_WORKSPACE;
+  std::vector<AdamTensor> ts(static_cast<size_t>(n));
+  long long chunks = 0;
+  for (int i = 0; i < n; ++i) {
+    if (numel[i] < 0) return DMUON_ERR_INVALID_ARG;
+    AdamTensor& T = ts[i];
+    T.numel = numel[i];
+    T.chunk_begin = chunks;
+    chunks += ceil_div(numel[i], kChunk);
+    if (numel[i] == 0) continue;
+    if (param[i] == nullptr || grad[i] == nullptr || exp_avg[i] == nullptr ||
+        exp_avg_sq[i] == nullptr)
+      return DMUON_ERR_INVALID_ARG;
+    T.p = param[i];
+    T.g = grad[i];
+    T.m = exp_avg[i];
+    T.v = exp_avg_sq[i];
+    T.vec = (aligned(T.p, 16) && aligned(T.g, 16) && aligned(T.m, 16) && aligned(T.v, 16)) ? 1 : 0;
+  }
+  if (chunks == 0) return DMUON_OK;
+  DevInfo D;
+  const int st = device_info(&D);
+  if (st != DMUON_OK) return st;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  const size_t bytes = align_up(size_t(n) * sizeof(AdamTensor), 16);
+  std::vector<unsigned char> blob(bytes, 0);
+  std::memcpy(blob.data(), ts.data(), size_t(n) * sizeof(AdamTensor));
+  if (launch_upload(ws + kHdrBytes, blob.data(), bytes, stream) != cudaSuccess)
+    return DMUON_ERR_CUDA;
+  // per-step scalars in double on the host, each rounded to fp32 once
+  const double bc1 = 1.0 - std::pow(beta1, double(step));
+  const double bc2 = 1.0 - std::pow(beta2, double(step));
+  AdamScalars k;
+  k.b1 = float(beta1);
+  k.b2 = float(beta2);
+  k.omb1 = float(1.0 - beta1);
+  k.omb2 = float(1.0 - beta2);
+  k.step_size = float(lr / bc1);
+  k.inv_bc2_sqrt = float(1.0 / std::sqrt(bc2));
+  k.eps = float(eps);
+  k.decay = float(1.0 - lr * weight_decay);
+  if (launch_adamw(reinterpret_cast<const AdamTensor*>(ws + kHdrBytes), n, chunks,
+                   param_dt == DMUON_BF16, grad_dt == DMUON_BF16, k, stream) != cudaSuccess)
+    return DMUON_ERR_CUDA;
+  return DMUON_OK;
+}
+
 int dmuon_stream_status(cudaStream_t stream, void* workspace) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return DMUON_ERR_CUDA;
   if (workspace == nullptr) return DMUON_OK;
@@ -745,5 +825,11 @@ const char* dmuon_status_string(int status) {
 }
 
 int dmuon_version(void) { return 100; }
+
+long long dmuon_launch_count(int reset) {
+  const long long n = t_launches;
+  if (reset) t_launches = 0;
+  return n;
+}
 
 }  // extern "C"

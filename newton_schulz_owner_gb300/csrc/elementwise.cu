@@ -339,6 +339,94 @@ __global__ void __launch_bounds__(kEwThreads) update_kernel(const EwMat* __restr
   }
 }
 
+DM_DEV int find_adam(const AdamTensor* t, int n, long long chunk) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (t[mid].chunk_begin <= chunk) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <bool BF16>
+DM_DEV void load8(const void* base, long long e, float (&f)[8]) {
+  if (BF16) {
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(base) + e),
+                  f);
+  } else {
+    const float4* q = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + e);
+    const float4 a = q[0], b = q[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+}
+
+template <bool BF16>
+DM_DEV float load1(const void* base, long long e) {
+  return BF16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[e])
+              : reinterpret_cast<const float*>(base)[e];
+}
+
+DM_DEV void store8f(float* base, long long e, const float (&f)[8]) {
+  float4* q = reinterpret_cast<float4*>(base + e);
+  q[0] = make_float4(f[0], f[1], f[2], f[3]);
+  q[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+// AdamW with decoupled weight decay, fp32 arithmetic:
+//   p <- p * decay;  m <- b1 m + (1-b1) g;  v <- b2 v + (1-b2) g^2;
+//   p <- p - step_size * m / (sqrt(v) * inv_bc2_sqrt + eps)
+template <bool P_BF16, bool G_BF16>
+__global__ void __launch_bounds__(kEwThreads) adamw_kernel(const AdamTensor* __restrict__ ts,
+                                                           int n, AdamScalars ks) {
+  const long long chunk = blockIdx.x;
+  const AdamTensor& T = ts[find_adam(ts, n, chunk)];
+  const long long start = (chunk - T.chunk_begin) * kChunk;
+  const long long end = min(T.numel, start + kChunk);
+  const float b1 = ks.b1, b2 = ks.b2, omb1 = ks.omb1, omb2 = ks.omb2;
+  const float decay = ks.decay, step_size = ks.step_size, inv_bc2_sqrt = ks.inv_bc2_sqrt;
+  const float eps = ks.eps;
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const long long e = start + (long long)(it * kEwThreads + threadIdx.x) * kVec;
+    if (e >= end) break;
+    if (T.vec && e + kVec <= end) {
+      float p[kVec], g[kVec], m[kVec], v[kVec];
+      load8<P_BF16>(T.p, e, p);
+      load8<G_BF16>(T.g, e, g);
+      load8<false>(T.m, e, m);
+      load8<false>(T.v, e, v);
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) {
+        m[k] = fmaf(b1, m[k], omb1 * g[k]);
+        v[k] = fmaf(b2, v[k], omb2 * g[k] * g[k]);
+        const float denom = fmaf(sqrtf(v[k]), inv_bc2_sqrt, eps);
+        p[k] = fmaf(-step_size, m[k] / denom, p[k] * decay);
+      }
+      store8f(T.m, e, m);
+      store8f(T.v, e, v);
+      if (P_BF16)
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(T.p) + e) = f32x8_to_bf16x8(p);
+      else
+        store8f(reinterpret_cast<float*>(T.p), e, p);
+    } else {
+      for (int k = 0; k < kVec && e + k < end; ++k) {
+        const long long i = e + k;
+        const float g = load1<G_BF16>(T.g, i);
+        const float m = fmaf(b1, T.m[i], omb1 * g);
+        const float v = fmaf(b2, T.v[i], omb2 * g * g);
+        const float denom = fmaf(sqrtf(v), inv_bc2_sqrt, eps);
+        const float p = fmaf(-step_size, m / denom, load1<P_BF16>(T.p, i) * decay);
+        T.m[i] = m;
+        T.v[i] = v;
+        if (P_BF16) reinterpret_cast<__nv_bfloat16*>(T.p)[i] = __float2bfloat16_rn(p);
+        else reinterpret_cast<float*>(T.p)[i] = p;
+      }
+    }
+  }
+}
+
 // Kernel-parameter payload for table uploads (kernel parameters may hold up to
 // 32764 bytes).
 constexpr int kUploadBytes = 30720;
@@ -383,7 +471,7 @@ cudaError_t launch_upload(void* dst, const void* src, size_t bytes, cudaStream_t
     a.pad_ = 0;
     memcpy(a.data, p + off, nb);
     upload_kernel<<<1, 256, 0, s>>>(a);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = counted(cudaGetLastError());
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -399,35 +487,35 @@ cudaError_t launch_momentum_pack(const EwMat* ew, int n, long long total_chunks,
   else
     momentum_pack_kernel<false><<<grid_of(total_chunks), kEwThreads, 0, s>>>(ew, n, beta, packed,
                                                                              partials);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_norm_partials(const EwMat* ew, int n, long long total_chunks,
                                  const __nv_bfloat16* packed, float* partials, cudaStream_t s) {
   if (total_chunks <= 0) return cudaSuccess;
   norm_partials_kernel<<<grid_of(total_chunks), kEwThreads, 0, s>>>(ew, n, packed, partials);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_norm_finalize(const EwMat* ew, int n, const float* partials, float eps,
                                  float* inv_norm, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   norm_finalize_kernel<<<n, kEwThreads, 0, s>>>(ew, partials, eps, inv_norm);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_relayout(const EwMat* ew, int n, long long total_tiles,
                             const __nv_bfloat16* packed, const float* inv_norm, cudaStream_t s) {
   if (total_tiles <= 0) return cudaSuccess;
   relayout_kernel<<<grid_of(total_tiles), kEwThreads, 0, s>>>(ew, n, packed, inv_norm);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_scale_inplace(const EwMat* ew, int n, long long total_chunks,
                                  __nv_bfloat16* packed, const float* inv_norm, cudaStream_t s) {
   if (total_chunks <= 0) return cudaSuccess;
   scale_inplace_kernel<<<grid_of(total_chunks), kEwThreads, 0, s>>>(ew, n, packed, inv_norm);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_update(const EwMat* ew, int n, long long total_chunks, bool weight_bf16,
@@ -437,12 +525,27 @@ cudaError_t launch_update(const EwMat* ew, int n, long long total_chunks, bool w
     update_kernel<true><<<grid_of(total_chunks), kEwThreads, 0, s>>>(ew, n, lr, packed);
   else
     update_kernel<false><<<grid_of(total_chunks), kEwThreads, 0, s>>>(ew, n, lr, packed);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
+}
+
+cudaError_t launch_adamw(const AdamTensor* ts, int n, long long total_chunks, bool p_bf16,
+                         bool g_bf16, const AdamScalars& k, cudaStream_t s) {
+  if (total_chunks <= 0) return cudaSuccess;
+  const unsigned grid = grid_of(total_chunks);
+  if (p_bf16 && g_bf16)
+    adamw_kernel<true, true><<<grid, kEwThreads, 0, s>>>(ts, n, k);
+  else if (p_bf16)
+    adamw_kernel<true, false><<<grid, kEwThreads, 0, s>>>(ts, n, k);
+  else if (g_bf16)
+    adamw_kernel<false, true><<<grid, kEwThreads, 0, s>>>(ts, n, k);
+  else
+    adamw_kernel<false, false><<<grid, kEwThreads, 0, s>>>(ts, n, k);
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_wait_timeout(int* err, long long budget_cycles, cudaStream_t s) {
   wait_timeout_kernel<<<1, 32, 0, s>>>(err, budget_cycles);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 }  // namespace dm

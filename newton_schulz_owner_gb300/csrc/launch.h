@@ -7,6 +7,14 @@
 
 namespace dm {
 
+// Every successful kernel launch of the library is counted per host thread
+// (read through dmuon_launch_count).
+void note_launch(int kernels = 1);
+inline cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) note_launch();
+  return e;
+}
+
 // ns_gemm.cu
 size_t ns_gemm_smem_bytes();
 // Once per device: opt into large shared memory and find how many CTA pairs
@@ -36,5 +44,7 @@ cudaError_t launch_scale_inplace(const EwMat* ew, int n, long long total_chunks,
 cudaError_t launch_update(const EwMat* ew, int n, long long total_chunks, bool weight_bf16,
                           float lr, const __nv_bfloat16* packed, cudaStream_t s);
 cudaError_t launch_wait_timeout(int* err, long long budget_cycles, cudaStream_t s);
+cudaError_t launch_adamw(const AdamTensor* ts, int n, long long total_chunks, bool p_bf16,
+                         bool g_bf16, const AdamScalars& k, cudaStream_t s);
 
 }  // namespace dm

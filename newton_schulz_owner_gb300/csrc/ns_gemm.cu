@@ -487,7 +487,7 @@ cudaError_t launch_diag_shift(const Bucket* buckets, int n_buckets, int first_in
                               cudaStream_t s) {
   if (n_mats <= 0) return cudaSuccess;
   diag_shift_kernel<<<n_mats, 256, 0, s>>>(buckets, n_buckets, first_internal, slot, b, c, shift);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 size_t ns_gemm_smem_bytes() { return kSmemBytes; }
@@ -517,8 +517,8 @@ cudaError_t launch_ns_gemm(const GemmArgs& g, bool full, int max_clusters, cudaS
   const int clusters = g.total_tiles < max_clusters ? g.total_tiles : max_clusters;
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg = pair_config(clusters, s, &attr);
-  if (full) return cudaLaunchKernelEx(&cfg, ns_gemm_kernel<true>, g);
-  return cudaLaunchKernelEx(&cfg, ns_gemm_kernel<false>, g);
+  if (full) return counted(cudaLaunchKernelEx(&cfg, ns_gemm_kernel<true>, g));
+  return counted(cudaLaunchKernelEx(&cfg, ns_gemm_kernel<false>, g));
 }
 
 }  // namespace dm

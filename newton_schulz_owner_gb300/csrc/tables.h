@@ -60,6 +60,27 @@ struct Bucket {
   int pad_;
 };
 
+// One tensor of an AdamW group (any shape, contiguous), walked in chunks.
+struct AdamTensor {
+  void* p;                 // parameter (bf16 or fp32)
+  const void* g;           // gradient (bf16 or fp32)
+  float* m;                // first moment
+  float* v;                // second moment
+  long long numel;
+  long long chunk_begin;
+  int vec;                 // all four pointers 16-byte aligned
+  int pad_;
+};
+
+// Per-step AdamW scalars, formed in double on the host and rounded once.
+struct AdamScalars {
+  float b1, b2, omb1, omb2;      // beta1, beta2, 1 - beta1, 1 - beta2
+  float step_size;               // lr / (1 - beta1^t)
+  float inv_bc2_sqrt;            // 1 / sqrt(1 - beta2^t)
+  float eps;
+  float decay;                   // 1 - lr * weight_decay
+};
+
 // Internal (bucket-major) order -> caller matrix.
 struct InternalMat {
   long long packed_off;

@@ -28,8 +28,9 @@ DEFAULT_ABC = (3.4445, -4.7750, 2.0315)
 
 EXPORTED = ("dmuon_plan", "dmuon_workspace_bytes", "dmuon_pack", "dmuon_ns_batched",
             "dmuon_unpack_update", "dmuon_muon_step", "dmuon_stream_status",
-            "dmuon_debug_wait_timeout", "dmuon_ns_batched_noalloc", "dmuon_status_string",
-            "dmuon_version")
+            "dmuon_debug_wait_timeout", "dmuon_ns_batched_noalloc", "dmuon_adamw",
+            "dmuon_adamw_workspace_bytes", "dmuon_status_string", "dmuon_version",
+            "dmuon_launch_count")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -59,6 +60,12 @@ _lib.dmuon_muon_step.restype = _i
 _lib.dmuon_ns_batched_noalloc.argtypes = [_i, _ShapeP, _vp, _i64p, _i, _i,
                                           ctypes.POINTER(ctypes.c_float), _f, _vp]
 _lib.dmuon_ns_batched_noalloc.restype = _i
+_lib.dmuon_adamw_workspace_bytes.argtypes = [_i]
+_lib.dmuon_adamw_workspace_bytes.restype = _sz
+_d = ctypes.c_double
+_lib.dmuon_adamw.argtypes = [_i, _i64p, _VPP, _i, _VPP, _i, _VPP, _VPP, _d, _d, _d, _d, _d, _i,
+                             _vp, _sz, _vp]
+_lib.dmuon_adamw.restype = _i
 _lib.dmuon_stream_status.argtypes = [_vp, _vp]
 _lib.dmuon_stream_status.restype = _i
 _lib.dmuon_debug_wait_timeout.argtypes = [_vp, _sz, _i, _vp]
@@ -67,6 +74,8 @@ _lib.dmuon_status_string.argtypes = [_i]
 _lib.dmuon_status_string.restype = ctypes.c_char_p
 _lib.dmuon_version.argtypes = []
 _lib.dmuon_version.restype = _i
+_lib.dmuon_launch_count.argtypes = [_i]
+_lib.dmuon_launch_count.restype = ctypes.c_longlong
 
 
 class DMuonError(RuntimeError):
@@ -89,6 +98,11 @@ def status_string(status: int) -> str:
 
 def version() -> int:
     return int(_lib.dmuon_version())
+
+
+def launch_count(reset: bool = False) -> int:
+    """Kernels the library launched from this host thread since the last reset."""
+    return int(_lib.dmuon_launch_count(1 if reset else 0))
 
 
 def _check(status: int, where: str) -> None:
@@ -201,6 +215,24 @@ def muon_step(shapes, grads, momenta, weights, packed, offsets, workspace, lr: f
                                 _ptrs(weights), wdt, float(lr), float(beta), int(ns_steps),
                                 int(variant), _addr(packed), _i64(offsets), _addr(workspace),
                                 workspace.numel(), _stream(stream)), "dmuon_muon_step")
+
+
+def adamw_workspace_bytes(n: int) -> int:
+    return int(_lib.dmuon_adamw_workspace_bytes(int(n)))
+
+
+def adamw(params, grads, exp_avgs, exp_avg_sqs, step: int, workspace, lr: float = 1e-3,
+          betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.01,
+          stream=None) -> None:
+    """One AdamW step over a list of tensors (one kernel launch)."""
+    n = len(params)
+    pdt = _dtype(params[0]) if n else F32
+    gdt = _dtype(grads[0]) if n else F32
+    numel = _i64([p.numel() for p in params])
+    _check(_lib.dmuon_adamw(n, numel, _ptrs(params), pdt, _ptrs(grads), gdt, _ptrs(exp_avgs),
+                            _ptrs(exp_avg_sqs), float(lr), float(betas[0]), float(betas[1]),
+                            float(eps), float(weight_decay), int(step), _addr(workspace),
+                            workspace.numel(), _stream(stream)), "dmuon_adamw")
 
 
 def stream_status(workspace=None, stream=None) -> int:

@@ -41,6 +41,8 @@ class Workload:
     grad_std: float = 1e-3
     weight_std: float = 0.02
     n_owners: int = 1
+    vocab: int = 0                   # embedding rows (0: no AdamW parameters)
+    tied_head: bool = False          # output head shares the embedding
 
     def shapes(self) -> List[Shape]:
         out: List[Shape] = []
@@ -48,6 +50,19 @@ class Workload:
             for p in _PROJ_ORDER:
                 if p in self.layer_shapes:
                     out.append(self.layer_shapes[p])
+        return out
+
+    def adamw_shapes(self) -> List[Shape]:
+        """Parameters outside the Muon set, updated by AdamW: token embedding,
+        output head (when not tied to the embedding), and the RMSNorm weights
+        (two per layer plus the final one), as (rows, cols)."""
+        if self.vocab <= 0:
+            return []
+        hidden = self.layer_shapes["q"][1]
+        out = [(self.vocab, hidden)]
+        if not self.tied_head:
+            out.append((self.vocab, hidden))
+        out += [(1, hidden)] * (2 * self.layers + 1)
         return out
 
     def names(self) -> List[str]:
@@ -64,10 +79,12 @@ WORKLOADS: Dict[str, Workload] = {
     "single-256x1024": Workload("single-256x1024", 0, 1, {"q": (256, 1024)},
                                 grad_dtype=torch.float32, weight_dtype=torch.float32,
                                 grad_std=1.0, weight_std=0.02),
-    "qwen2.5-1.5b": Workload("qwen2.5-1.5b", 1, 28, _layer(1536, 256, 8960)),
-    "llama-3.2-3b": Workload("llama-3.2-3b", 2, 28, _layer(3072, 1024, 8192), n_owners=8),
-    "llama-3.1-8b": Workload("llama-3.1-8b", 3, 32, _layer(4096, 1024, 14336)),
-    "qwen2.5-7b": Workload("qwen2.5-7b", 4, 28, _layer(3584, 512, 18944)),
+    "qwen2.5-1.5b": Workload("qwen2.5-1.5b", 1, 28, _layer(1536, 256, 8960),
+                             vocab=151936, tied_head=True),
+    "llama-3.2-3b": Workload("llama-3.2-3b", 2, 28, _layer(3072, 1024, 8192), n_owners=8,
+                             vocab=128256, tied_head=True),
+    "llama-3.1-8b": Workload("llama-3.1-8b", 3, 32, _layer(4096, 1024, 14336), vocab=128256),
+    "qwen2.5-7b": Workload("qwen2.5-7b", 4, 28, _layer(3584, 512, 18944), vocab=152064),
     # One layer of the Llama-3.1-8B set (7 matrices, 218 M elements, ~3.5 GB on
     # the device with workspace): the same kernels on a case small enough for
     # multi-pass profiler captures.

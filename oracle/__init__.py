@@ -10,4 +10,5 @@ from .muon_oracle import (  # noqa: F401
     nesterov_momentum, ns_working_matrix, ns_normalise, newton_schulz,
     gram_newton_schulz, update_scale, apply_update, muon_step, round_bf16,
     lpt_assign, pack_plan, ns_flops_algorithmic, gram_ns_flops_algorithmic,
+    adamw_step, ADAMW_DEFAULT_LR, ADAMW_DEFAULT_BETAS, ADAMW_DEFAULT_EPS, ADAMW_DEFAULT_WD,
 )

@@ -170,6 +170,42 @@ def muon_step(G: np.ndarray, M: np.ndarray, W: np.ndarray, lr: float = DEFAULT_L
 
 
 # ---------------------------------------------------------------------------
+# AdamW for the parameters Muon does not own
+# ---------------------------------------------------------------------------
+ADAMW_DEFAULT_LR = 1e-3          # home page, "LLM Pretraining": Muon(..., adamw_lr=1e-3)
+ADAMW_DEFAULT_BETAS = (0.9, 0.999)
+ADAMW_DEFAULT_EPS = 1e-8
+ADAMW_DEFAULT_WD = 0.01
+
+
+def adamw_step(p: np.ndarray, g: np.ndarray, m: np.ndarray, v: np.ndarray, step: int,
+               lr: float = ADAMW_DEFAULT_LR, betas: Tuple[float, float] = ADAMW_DEFAULT_BETAS,
+               eps: float = ADAMW_DEFAULT_EPS,
+               weight_decay: float = ADAMW_DEFAULT_WD) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """One AdamW step (decoupled weight decay), fp64.  Returns (p, m, v).
+
+    Home page, "LLM Pretraining": parameters outside the Muon set (embeddings,
+    norms, heads) use AdamW with ``adamw_lr``.  The pages give no other
+    hyper-parameter; the reading is the usual AdamW with decay applied to the
+    parameter before the moment update:
+      p <- p (1 - lr wd)
+      m <- b1 m + (1 - b1) g;   v <- b2 v + (1 - b2) g^2
+      p <- p - (lr / (1 - b1^t)) m / (sqrt(v) / sqrt(1 - b2^t) + eps)
+    """
+    if step < 1:
+        raise ValueError("step counts from 1")
+    b1, b2 = betas
+    p = np.asarray(p, np.float64) * (1.0 - lr * weight_decay)
+    g = np.asarray(g, np.float64)
+    m = b1 * np.asarray(m, np.float64) + (1.0 - b1) * g
+    v = b2 * np.asarray(v, np.float64) + (1.0 - b2) * g * g
+    bc1 = 1.0 - b1 ** step
+    bc2 = 1.0 - b2 ** step
+    p = p - (lr / bc1) * m / (np.sqrt(v) / math.sqrt(bc2) + eps)
+    return p, m, v
+
+
+# ---------------------------------------------------------------------------
 # bf16 round-to-nearest-even, from the IEEE definition
 # ---------------------------------------------------------------------------
 _BF16_MANT_BITS = 7          # explicit fraction bits

@@ -299,3 +299,38 @@ def test_planted_ns_mistakes_fail_the_pins(kind):
     assert bad, kind
     # the unmutated copy passes, so the check itself is not vacuous
     assert _rel(_ns_mutant("none")(G, 5), svd_closed_form(G, 5)) < 1e-12
+
+
+# ------------------------------------------------------------------ AdamW
+def test_adamw_matches_torch_optim_adamw():
+    rng = np.random.default_rng(4)
+    p0 = rng.standard_normal((7, 33))
+    grads = [rng.standard_normal((7, 33)) for _ in range(4)]
+    tp = torch.nn.Parameter(torch.tensor(p0, dtype=torch.float64))
+    opt = torch.optim.AdamW([tp], lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01)
+    p, m, v = p0.copy(), np.zeros_like(p0), np.zeros_like(p0)
+    for t, g in enumerate(grads, start=1):
+        tp.grad = torch.tensor(g, dtype=torch.float64)
+        opt.step()
+        p, m, v = oracle.adamw_step(p, g, m, v, t)
+        assert np.allclose(p, tp.detach().numpy(), rtol=1e-13, atol=1e-15)
+        st = opt.state[tp]
+        assert np.allclose(m, st["exp_avg"].numpy(), rtol=1e-13, atol=0)
+        assert np.allclose(v, st["exp_avg_sq"].numpy(), rtol=1e-13, atol=0)
+
+
+def test_adamw_constant_gradient_closed_form():
+    # with a constant gradient the bias-corrected moments are exactly g and g^2,
+    # so each step moves p by lr * g / (|g| + eps) after the decay
+    g = np.array([[0.5, -2.0, 3e-3]])
+    p = np.array([[1.0, 1.0, -1.0]])
+    m = v = np.zeros_like(g)
+    for t in range(1, 6):
+        p_dec = p * (1 - 1e-3 * 0.01)
+        p, m, v = oracle.adamw_step(p, g, m, v, t)
+        assert np.allclose(p, p_dec - 1e-3 * g / (np.abs(g) + 1e-8), rtol=1e-12, atol=1e-15)
+
+
+def test_adamw_defaults_golden():
+    assert oracle.ADAMW_DEFAULT_LR == json.load(open(os.path.join(GOLD, "muon_constants.json")))[
+        "adamw_lr"]["value"]
