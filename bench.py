@@ -204,6 +204,22 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------- GPU arm
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """Largest value over all ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def owned_matrices(shapes, rank: int, world: int):
+    """Indices of the matrices rank `rank` owns when `world` ranks split the set
+    with the library's owner plan (each matrix has exactly one owner)."""
+    from newton_schulz_owner_gb300 import dmuon
+    owner_of, _, _ = dmuon.plan(shapes, world)
+    return [i for i, o in enumerate(owner_of) if o == rank]
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -293,11 +309,7 @@ def run_gpu(args, rank, world, local_rank):
     pack_ms = [e[0].elapsed_time(e[1]) for e in evs]
     ns_ms = [e[1].elapsed_time(e[2]) for e in evs]
     upd_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    t_total = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([t_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_total = float(t.item())
+    t_total = max_over_ranks(sum(step_ms), dist, dev)
     ms = t_total / args.steps
     ns_mean = sum(ns_ms) / len(ns_ms)
     achieved_tflops = ns_flops / (ns_mean * 1e-3) / 1e12
@@ -398,11 +410,7 @@ def run_gpu(args, rank, world, local_rank):
         st = dmuon.stream_status(owner.workspace, stream)
         if st != dmuon.OK:
             raise RuntimeError(f"e2e steps failed: {dmuon.status_string(st)}")
-        e2e_ms = e0.elapsed_time(e1) / args.steps
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
         e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h)}
         del G_host, W_host, G_dev, W_snap
