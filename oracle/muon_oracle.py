@@ -40,7 +40,8 @@ this file): SVD closed form of the quintic, scalar brute force on 1x1 / 1xn /
 diagonal cases, singular-value band, rotation invariance, transpose symmetry,
 momentum closed form for a constant gradient, RNE bf16 rounding against the
 IEEE definition, LPT hand-worked case plus the Graham bound against brute force
-optimum.  Every function below is pinned; none is "parity unpinned".
+optimum, AdamW against torch.optim.AdamW (fp64) and its constant-gradient closed
+form.  Every function below is pinned; none is "parity unpinned".
 """
 from __future__ import annotations
 
