@@ -446,7 +446,8 @@ def run_gpu(args, rank, world, local_rank):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     phases = {
         "note": "three-call decomposition (pack, ns_batched, unpack_update) timed in a second "
-                "region; dmuon_muon_step (the value) fuses the update into the last product",
+                "region, each phase alone; dmuon_muon_step (the value) overlaps the "
+                "memory-bound phases with the products on a second stream",
         "pack_ms": pack_mean, "ns_ms": ns_mean, "update_ms": upd_mean,
         "three_call_step_ms": sum(e[0].elapsed_time(e[3]) for e in evs) / len(evs),
         "pack_gbs": elems * elem_bytes["pack"] / (pack_mean * 1e-3) / 1e9,

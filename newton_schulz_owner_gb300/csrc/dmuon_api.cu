@@ -39,6 +39,9 @@ struct BucketPlan {
   size_t slot_off[kSlots] = {};
   std::vector<int> sym;   // (ti << 16) | tj, upper-triangle tiles of an m x m product
   int full_ti = 0, full_tj = 0;
+  int first = 0;                    // table position of the first matrix
+  long long chunk_lo = 0, chunks = 0, tile_lo = 0, tiles = 0;  // its elementwise work
+  int sym_begin = 0, full_begin = 0;  // first product tile of the bucket within its group
 };
 
 struct Plan {
@@ -46,8 +49,10 @@ struct Plan {
   std::vector<BucketPlan> buckets;  // standard buckets first, then Gram buckets
   int n_std = 0;                    // number of standard buckets
   std::vector<int> bucket_of, idx_in_bucket, internal_of;
-  std::vector<long long> chunk_begin, tile_begin;
-  std::vector<int> n_chunks, tiles_r, tiles_c;
+  std::vector<long long> chunk_begin, tile_begin;  // per caller matrix
+  std::vector<int> n_chunks, tiles_r, tiles_c;     // per caller matrix
+  std::vector<int> ew_order;                        // table position -> caller matrix
+  std::vector<int> ew_pos;                          // caller matrix -> table position
   long long total_chunks = 0, total_tiles = 0;
   int n_internal = 0;
   int sym_total = 0;
@@ -85,8 +90,11 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
   P.tiles_r.assign(n, 0);
   P.tiles_c.assign(n, 0);
 
-  // buckets keyed by (gram, m, n); standard first, each group in first-seen order
+  // buckets keyed by (gram, m, n); standard first, each group in first-seen
+  // order, except that the standard bucket with the most elements goes last
+  // (a whole step overlaps its memory-bound work with the others' products)
   std::map<std::tuple<int, int, int>, int> key_to_b;
+  std::map<std::tuple<int, int, int>, long long> key_elems;
   std::vector<std::tuple<int, int, int>> order;
   for (int i = 0; i < n; ++i) {
     if (!shape_ok(shp[i])) return DMUON_ERR_INVALID_ARG;
@@ -94,10 +102,6 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
     P.n_chunks[i] = int(ceil_div(r * c, kChunk));
     P.tiles_r[i] = int(ceil_div(r, kRelayTile));
     P.tiles_c[i] = int(ceil_div(c, kRelayTile));
-    P.chunk_begin[i] = P.total_chunks;
-    P.tile_begin[i] = P.total_tiles;
-    P.total_chunks += P.n_chunks[i];
-    P.total_tiles += (long long)P.tiles_r[i] * P.tiles_c[i];
     if (r == 0 || c == 0) continue;
     const int m = int(std::min(r, c)), nn = int(std::max(r, c));
     const auto key = std::make_tuple(uses_gram(variant, m, nn) ? 1 : 0, m, nn);
@@ -105,9 +109,19 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
       key_to_b[key] = -1;
       order.push_back(key);
     }
+    key_elems[key] += r * c;
   }
   std::stable_sort(order.begin(), order.end(),
                    [](const auto& a, const auto& b) { return std::get<0>(a) < std::get<0>(b); });
+  {
+    int n_std = 0, big = -1;
+    for (size_t b = 0; b < order.size(); ++b) {
+      if (std::get<0>(order[b]) != 0) break;
+      ++n_std;
+      if (big < 0 || key_elems[order[b]] > key_elems[order[size_t(big)]]) big = int(b);
+    }
+    if (big >= 0) std::rotate(order.begin() + big, order.begin() + big + 1, order.begin() + n_std);
+  }
   for (size_t b = 0; b < order.size(); ++b) {
     key_to_b[order[b]] = int(b);
     BucketPlan bp;
@@ -148,6 +162,42 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
     P.sym_total += int(B.sym.size());
   }
   P.n_internal = internal;
+
+  // The per-matrix table follows the internal (bucket-major) order, empty
+  // matrices last, so that every bucket -- and every run of buckets -- is one
+  // contiguous range of table entries, chunks and relayout tiles.
+  P.ew_pos.assign(n, -1);
+  for (const auto& B : P.buckets)
+    for (int i : B.mats) P.ew_order.push_back(i);
+  for (int i = 0; i < n; ++i)
+    if (P.bucket_of[i] < 0) P.ew_order.push_back(i);
+  for (int k = 0; k < n; ++k) {
+    const int i = P.ew_order[k];
+    P.ew_pos[i] = k;
+    P.chunk_begin[i] = P.total_chunks;
+    P.tile_begin[i] = P.total_tiles;
+    P.total_chunks += P.n_chunks[i];
+    P.total_tiles += (long long)P.tiles_r[i] * P.tiles_c[i];
+  }
+  // product tile numbering: one sequence over the standard buckets, another
+  // over the Gram buckets (each group's launches start at its first bucket)
+  long long sym_begin = 0, full_begin = 0;
+  for (size_t b = 0; b < P.buckets.size(); ++b) {
+    BucketPlan& B = P.buckets[b];
+    if (int(b) == P.n_std) sym_begin = full_begin = 0;
+    B.first = P.ew_pos[B.mats.front()];
+    B.chunk_lo = P.chunk_begin[B.mats.front()];
+    B.tile_lo = P.tile_begin[B.mats.front()];
+    for (int i : B.mats) {
+      B.chunks += P.n_chunks[i];
+      B.tiles += (long long)P.tiles_r[i] * P.tiles_c[i];
+    }
+    B.sym_begin = int(sym_begin);
+    B.full_begin = int(full_begin);
+    sym_begin += (long long)B.mats.size() * (long long)B.sym.size();
+    full_begin += (long long)B.mats.size() * B.full_ti * B.full_tj;
+    if (sym_begin > INT32_MAX || full_begin > INT32_MAX) return DMUON_ERR_UNSUPPORTED;
+  }
 
   // workspace layout
   size_t off = kHdrBytes;
@@ -190,6 +240,9 @@ struct DevInfo {
   int sms = 0;
   int clock_khz = 0;
   int max_clusters = 0;  // resident CTA pairs of the product kernel
+  // Lowest-priority stream on which a whole step runs its memory-bound kernels
+  // next to the products (null: the step runs on the caller's stream alone).
+  cudaStream_t aux = nullptr;
 };
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
@@ -211,6 +264,13 @@ int device_info(DevInfo* out) {
       D.status = DMUON_ERR_UNSUPPORTED;
     } else if (ns_gemm_prepare(D.sms, &D.max_clusters) != cudaSuccess) {
       return DMUON_ERR_CUDA;
+    } else {
+      int least = 0, greatest = 0;
+      if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+          cudaStreamCreateWithPriority(&D.aux, cudaStreamNonBlocking, least) != cudaSuccess) {
+        D.aux = nullptr;
+        (void)cudaGetLastError();
+      }
     }
     D.ready = true;
   }
@@ -315,7 +375,7 @@ int upload_tables(const Request& R, const Plan& P) {
   CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(at(P.off_tmaps));
 
   for (int i = 0; i < P.n; ++i) {
-    EwMat& E = ew[i];
+    EwMat& E = ew[P.ew_pos[i]];
     const long long r = R.shp[i].rows, c = R.shp[i].cols;
     E.rows = int(r);
     E.cols = int(c);
@@ -352,10 +412,8 @@ int upload_tables(const Request& R, const Plan& P) {
     }
   }
   int sym_off = 0, internal = 0;
-  int sym_begin = 0, full_begin = 0;
   for (size_t b = 0; b < P.buckets.size(); ++b) {
     const BucketPlan& BP = P.buckets[b];
-    if (int(b) == P.n_std) sym_begin = full_begin = 0;  // Gram buckets start a new launch group
     Bucket& B = bk[b];
     B.m = BP.m;
     B.n = BP.n;
@@ -382,35 +440,37 @@ int upload_tables(const Request& R, const Plan& P) {
     sym_off += B.sym_count;
     B.full_ti = BP.full_ti;
     B.full_tj = BP.full_tj;
-    B.sym_begin = sym_begin;
-    B.full_begin = full_begin;
-    sym_begin += B.count * B.sym_count;
-    full_begin += B.count * B.full_ti * B.full_tj;
+    B.sym_begin = BP.sym_begin;
+    B.full_begin = BP.full_begin;
   }
   if (launch_upload(ws + P.off_tables, blob.data(), blob.size(), R.stream) != cudaSuccess)
     return DMUON_ERR_CUDA;
   return DMUON_OK;
 }
 
-// Total tiles of a launch over buckets [b0, b1).
-void group_tiles(const Plan& P, int b0, int b1, int* sym_tiles, int* full_tiles) {
-  long long s = 0, f = 0;
-  for (int b = b0; b < b1; ++b) {
-    const BucketPlan& B = P.buckets[b];
-    s += (long long)B.mats.size() * B.sym.size();
-    f += (long long)B.mats.size() * B.full_ti * B.full_tj;
-  }
-  *sym_tiles = int(s);
-  *full_tiles = int(f);
-}
-
+// One run of Newton-Schulz product launches over the buckets [b0, b1) of one
+// group (standard or Gram), on `stream`.
 struct GemmLauncher {
   const Plan& P;
   const Request& R;
   int clusters;
   unsigned char* ws;
-  int b0 = 0, b1 = 0, sym_tiles = 0, full_tiles = 0;
+  int b0, b1;
+  cudaStream_t stream;
+  int sym_tiles = 0, full_tiles = 0;
 
+  GemmLauncher(const Plan& p, const Request& r, int c, unsigned char* w, int lo, int hi,
+               cudaStream_t s)
+      : P(p), R(r), clusters(c), ws(w), b0(lo), b1(hi), stream(s) {
+    long long st = 0, ft = 0;
+    for (int b = b0; b < b1; ++b) {
+      const BucketPlan& B = P.buckets[b];
+      st += (long long)B.mats.size() * B.sym.size();
+      ft += (long long)B.mats.size() * B.full_ti * B.full_tj;
+    }
+    sym_tiles = int(st);
+    full_tiles = int(ft);
+  }
   GemmArgs base() const {
     GemmArgs g{};
     g.buckets = reinterpret_cast<const Bucket*>(ws + P.off_bk) + b0;
@@ -427,26 +487,91 @@ struct GemmLauncher {
            const float* shift = nullptr, float shift_sign = 0.f) const {
     GemmArgs g = base();
     g.total_tiles = sym_tiles;
+    g.tile_base = P.buckets[b0].sym_begin;
     g.sL = sL; g.sR = sR; g.sAux = sAux; g.sOut = sOut;
     g.alpha = alpha; g.beta = beta; g.gamma = gamma;
     g.shift = shift; g.shift_sign = shift_sign;
-    return launch_ns_gemm(g, false, clusters, R.stream) == cudaSuccess;
+    return launch_ns_gemm(g, false, clusters, stream) == cudaSuccess;
   }
   // out = alpha*aux + gamma*L R  (m x n); final: write O into the packed buffer
   bool full(int sL, int sR, int sAux, int sOut, float alpha, float gamma, bool final,
             const float* shift = nullptr, float shift_sign = 0.f) const {
     GemmArgs g = base();
     g.total_tiles = full_tiles;
+    g.tile_base = P.buckets[b0].full_begin;
     g.sL = sL; g.sR = sR; g.sAux = sAux; g.sOut = sOut;
     g.alpha = alpha; g.beta = 0.f; g.gamma = gamma;
     g.shift = shift; g.shift_sign = shift_sign;
     g.final_out = final ? 1 : 0;
-    return launch_ns_gemm(g, true, clusters, R.stream) == cudaSuccess;
+    return launch_ns_gemm(g, true, clusters, stream) == cudaSuccess;
   }
+  int first() const { return P.buckets[b0].first; }
   int n_mats() const {
     int k = 0;
     for (int b = b0; b < b1; ++b) k += int(P.buckets[b].mats.size());
     return k;
+  }
+};
+
+// Standard Newton-Schulz on buckets [b0, b1), per step:
+//   A = X X^T;  d = b s + c s^2 with s = trace(A)/m;
+//   B' = b A + c A A - d I;  X' = (a + d) X + B' X   (= a X + B X)
+// Storing B' instead of B keeps B's large diagonal (about b + c once the
+// singular values approach 1) out of the bf16 rounding, where it would be
+// amplified by the cancellation between a X and B X.
+bool ns_standard(const GemmLauncher& L, const Request& R, const Plan& P, unsigned char* ws) {
+  const float a = R.abc[0], b = R.abc[1], c = R.abc[2];
+  float* shift = reinterpret_cast<float*>(ws + P.off_shift);
+  const Bucket* bk = reinterpret_cast<const Bucket*>(ws + P.off_bk) + L.b0;
+  for (int k = 0; k < R.ns_steps; ++k) {
+    const int xin = (k & 1) ? SX1 : SX0, xout = (k & 1) ? SX0 : SX1;
+    const bool last = k + 1 == R.ns_steps;
+    if (!L.sym(xin, xin, SM0, SM0, 0.f, 0.f, 1.f)) return false;
+    if (launch_diag_shift(bk, L.b1 - L.b0, L.first(), L.n_mats(), SM0, b, c, shift, L.stream) !=
+        cudaSuccess)
+      return false;
+    if (!L.sym(SM0, SM0, SM0, SM1, 0.f, b, c, shift, -1.f)) return false;
+    if (!L.full(SM1, xin, xin, xout, a, 1.f, last, shift, 1.f)) return false;
+  }
+  return true;
+}
+
+// Gram Newton-Schulz on buckets [b0, b1): A0 = X0 X0^T; per step
+// P = aI + bA + cA^2, Q = P Q, A' = A P^2; finally O = Q X0.  Slots: A in
+// SM0/SM1, P in SM2 (SM3 at step 0, where Q = P), Q in SM3/SM4, T = P^2 in SM5.
+bool ns_gram(const GemmLauncher& L, const Request& R) {
+  const float a = R.abc[0], b = R.abc[1], c = R.abc[2];
+  int sA = SM0, sAn = SM1, sQ = SM3, sQn = SM4;
+  if (!L.sym(SX0, SX0, SM0, sA, 0.f, 0.f, 1.f)) return false;
+  for (int k = 0; k < R.ns_steps; ++k) {
+    const bool last = k + 1 == R.ns_steps;
+    const int sP = (k == 0) ? SM3 : SM2;
+    if (!L.sym(sA, sA, sA, sP, a, b, c)) return false;
+    if (k > 0) {
+      if (!L.sym(sP, sQ, SM0, sQn, 0.f, 0.f, 1.f)) return false;
+      std::swap(sQ, sQn);
+    }
+    if (!last) {
+      if (!L.sym(sP, sP, SM0, SM5, 0.f, 0.f, 1.f)) return false;
+      if (!L.sym(sA, SM5, SM0, sAn, 0.f, 0.f, 1.f)) return false;
+      std::swap(sA, sAn);
+    }
+  }
+  return L.full(sQ, SX0, SX0, SX0, 0.f, 1.f, true);
+}
+
+// Events used to order the two streams of an overlapped step; released when
+// the call returns (the driver keeps a pending event alive until it fires).
+struct EventSet {
+  cudaEvent_t e[4] = {};
+  int made = 0;
+  bool create() {
+    for (; made < 4; ++made)
+      if (cudaEventCreateWithFlags(&e[made], cudaEventDisableTiming) != cudaSuccess) return false;
+    return true;
+  }
+  ~EventSet() {
+    for (int i = 0; i < made; ++i) cudaEventDestroy(e[i]);
   }
 };
 
@@ -471,81 +596,82 @@ int run(const Request& R) {
   float* inv = reinterpret_cast<float*>(ws + P.off_inv);
   __nv_bfloat16* packed = static_cast<__nv_bfloat16*>(R.packed);
   cudaStream_t s = R.stream;
+  const bool gbf16 = R.grad_dt == DMUON_BF16, wbf16 = R.weight_dt == DMUON_BF16;
+  const int nb = int(P.buckets.size());
+
+  // the whole table, and the part of it that belongs to buckets [b0, b1)
+  EwRange all{ew, R.n, 0, 0, P.total_chunks, 0, P.total_tiles};
+  auto range_of = [&](int b0, int b1) {
+    EwRange r{ew + P.buckets[b0].first, 0, P.buckets[b0].first, P.buckets[b0].chunk_lo, 0,
+              P.buckets[b0].tile_lo, 0};
+    for (int b = b0; b < b1; ++b) {
+      r.n += int(P.buckets[b].mats.size());
+      r.chunks += P.buckets[b].chunks;
+      r.tiles += P.buckets[b].tiles;
+    }
+    return r;
+  };
+
+  // A whole standard step over two or more buckets overlaps its memory-bound
+  // kernels with the products on a second, low-priority stream: the largest
+  // bucket (last) is packed and relaid out while the other buckets' products
+  // run, and the other buckets' weights are updated while its products run.
+  //   stream s : pack, norm, relayout of G1 | products G1 |   wait   | products G2, update G2 | join
+  //   aux      :                            | pack, norm, relayout G2 | update G1
+  const bool overlap = R.do_pack && R.do_ns && R.do_update && R.ns_steps > 0 && P.n_std >= 2 &&
+                       P.n_std == nb && D.aux != nullptr;
+  if (overlap) {
+    EventSet ev;
+    if (!ev.create()) return DMUON_ERR_CUDA;
+    const int split = P.n_std - 1;
+    const EwRange g1 = range_of(0, split), g2 = range_of(split, nb);
+    cudaStream_t x = D.aux;
+    if (launch_momentum_pack(g1, gbf16, R.beta, packed, partials, s) != cudaSuccess ||
+        launch_norm_finalize(g1, partials, R.eps, inv, s) != cudaSuccess ||
+        launch_relayout(g1, packed, inv, s) != cudaSuccess || cudaEventRecord(ev.e[0], s) != cudaSuccess)
+      return DMUON_ERR_CUDA;
+    if (cudaStreamWaitEvent(x, ev.e[0], 0) != cudaSuccess ||
+        launch_momentum_pack(g2, gbf16, R.beta, packed, partials, x) != cudaSuccess ||
+        launch_norm_finalize(g2, partials, R.eps, inv, x) != cudaSuccess ||
+        launch_relayout(g2, packed, inv, x) != cudaSuccess || cudaEventRecord(ev.e[1], x) != cudaSuccess)
+      return DMUON_ERR_CUDA;
+    if (!ns_standard(GemmLauncher(P, R, D.max_clusters, ws, 0, split, s), R, P, ws) ||
+        cudaEventRecord(ev.e[2], s) != cudaSuccess)
+      return DMUON_ERR_CUDA;
+    if (cudaStreamWaitEvent(x, ev.e[2], 0) != cudaSuccess ||
+        launch_update(g1, wbf16, R.lr, packed, x) != cudaSuccess ||
+        cudaEventRecord(ev.e[3], x) != cudaSuccess)
+      return DMUON_ERR_CUDA;
+    if (cudaStreamWaitEvent(s, ev.e[1], 0) != cudaSuccess ||
+        !ns_standard(GemmLauncher(P, R, D.max_clusters, ws, split, nb, s), R, P, ws) ||
+        launch_update(g2, wbf16, R.lr, packed, s) != cudaSuccess ||
+        cudaStreamWaitEvent(s, ev.e[3], 0) != cudaSuccess)
+      return DMUON_ERR_CUDA;
+    return DMUON_OK;
+  }
 
   if (R.do_pack) {
-    if (launch_momentum_pack(ew, R.n, P.total_chunks, R.grad_dt == DMUON_BF16, R.beta, packed,
-                             partials, s) != cudaSuccess)
+    if (launch_momentum_pack(all, gbf16, R.beta, packed, partials, s) != cudaSuccess)
       return DMUON_ERR_CUDA;
   }
   if (R.do_ns) {
     if (!R.do_pack && !R.pack_norms) {
-      if (launch_norm_partials(ew, R.n, P.total_chunks, packed, partials, s) != cudaSuccess)
-        return DMUON_ERR_CUDA;
+      if (launch_norm_partials(all, packed, partials, s) != cudaSuccess) return DMUON_ERR_CUDA;
     }
-    if (launch_norm_finalize(ew, R.n, partials, R.eps, inv, s) != cudaSuccess)
-      return DMUON_ERR_CUDA;
+    if (launch_norm_finalize(all, partials, R.eps, inv, s) != cudaSuccess) return DMUON_ERR_CUDA;
     if (R.ns_steps == 0) {
-      if (launch_scale_inplace(ew, R.n, P.total_chunks, packed, inv, s) != cudaSuccess)
-        return DMUON_ERR_CUDA;
+      if (launch_scale_inplace(all, packed, inv, s) != cudaSuccess) return DMUON_ERR_CUDA;
     } else {
-      if (launch_relayout(ew, R.n, P.total_tiles, packed, inv, s) != cudaSuccess)
+      if (launch_relayout(all, packed, inv, s) != cudaSuccess) return DMUON_ERR_CUDA;
+      if (P.n_std > 0 &&
+          !ns_standard(GemmLauncher(P, R, D.max_clusters, ws, 0, P.n_std, s), R, P, ws))
         return DMUON_ERR_CUDA;
-      const float a = R.abc[0], b = R.abc[1], c = R.abc[2];
-      // standard buckets, per step:
-      //   A = X X^T;  d = b s + c s^2 with s = trace(A)/m;
-      //   B' = b A + c A A - d I;  X' = (a + d) X + B' X   (= a X + B X)
-      // Storing B' instead of B keeps B's large diagonal (about b + c once the
-      // singular values approach 1) out of the bf16 rounding, where it would be
-      // amplified by the cancellation between a X and B X.
-      if (P.n_std > 0) {
-        GemmLauncher L{P, R, D.max_clusters, ws};
-        L.b0 = 0;
-        L.b1 = P.n_std;
-        group_tiles(P, L.b0, L.b1, &L.sym_tiles, &L.full_tiles);
-        float* shift = reinterpret_cast<float*>(ws + P.off_shift);
-        const Bucket* bk = reinterpret_cast<const Bucket*>(ws + P.off_bk);
-        for (int k = 0; k < R.ns_steps; ++k) {
-          const int xin = (k & 1) ? SX1 : SX0, xout = (k & 1) ? SX0 : SX1;
-          const bool last = k + 1 == R.ns_steps;
-          if (!L.sym(xin, xin, SM0, SM0, 0.f, 0.f, 1.f)) return DMUON_ERR_CUDA;
-          if (launch_diag_shift(bk, P.n_std, 0, L.n_mats(), SM0, b, c, shift, s) != cudaSuccess)
-            return DMUON_ERR_CUDA;
-          if (!L.sym(SM0, SM0, SM0, SM1, 0.f, b, c, shift, -1.f)) return DMUON_ERR_CUDA;
-          if (!L.full(SM1, xin, xin, xout, a, 1.f, last, shift, 1.f)) return DMUON_ERR_CUDA;
-        }
-      }
-      // Gram buckets: A0 = X0 X0^T; per step P = aI + bA + cA^2, Q = P Q,
-      // A' = A P^2; finally O = Q X0.  Slots: A in SM0/SM1, P in SM2 (SM3 at
-      // step 0, where Q = P), Q in SM3/SM4, T = P^2 in SM5.
-      if (P.n_std < int(P.buckets.size())) {
-        GemmLauncher L{P, R, D.max_clusters, ws};
-        L.b0 = P.n_std;
-        L.b1 = int(P.buckets.size());
-        group_tiles(P, L.b0, L.b1, &L.sym_tiles, &L.full_tiles);
-        int sA = SM0, sAn = SM1, sQ = SM3, sQn = SM4;
-        if (!L.sym(SX0, SX0, SM0, sA, 0.f, 0.f, 1.f)) return DMUON_ERR_CUDA;
-        for (int k = 0; k < R.ns_steps; ++k) {
-          const bool last = k + 1 == R.ns_steps;
-          const int sP = (k == 0) ? SM3 : SM2;
-          if (!L.sym(sA, sA, sA, sP, a, b, c)) return DMUON_ERR_CUDA;
-          if (k > 0) {
-            if (!L.sym(sP, sQ, SM0, sQn, 0.f, 0.f, 1.f)) return DMUON_ERR_CUDA;
-            std::swap(sQ, sQn);
-          }
-          if (!last) {
-            if (!L.sym(sP, sP, SM0, SM5, 0.f, 0.f, 1.f)) return DMUON_ERR_CUDA;
-            if (!L.sym(sA, SM5, SM0, sAn, 0.f, 0.f, 1.f)) return DMUON_ERR_CUDA;
-            std::swap(sA, sAn);
-          }
-        }
-        if (!L.full(sQ, SX0, SX0, SX0, 0.f, 1.f, true)) return DMUON_ERR_CUDA;
-      }
+      if (P.n_std < nb && !ns_gram(GemmLauncher(P, R, D.max_clusters, ws, P.n_std, nb, s), R))
+        return DMUON_ERR_CUDA;
     }
   }
   if (R.do_update) {
-    if (launch_update(ew, R.n, P.total_chunks, R.weight_dt == DMUON_BF16, R.lr, packed, s) !=
-        cudaSuccess)
-      return DMUON_ERR_CUDA;
+    if (launch_update(all, wbf16, R.lr, packed, s) != cudaSuccess) return DMUON_ERR_CUDA;
   }
   return DMUON_OK;
 }

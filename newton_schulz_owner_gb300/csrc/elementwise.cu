@@ -74,12 +74,15 @@ DM_DEV float block_sum(float v) {
   return s;  // valid in thread 0
 }
 
+// Every chunked kernel below works on the sub-range ew[0, n) of the per-matrix
+// table; `base` is the global index of its first chunk (tile for relayout).
 template <bool G_BF16>
 __global__ void __launch_bounds__(kEwThreads) momentum_pack_kernel(const EwMat* __restrict__ ew,
-                                                                   int n, float beta,
+                                                                   int n, long long base,
+                                                                   float beta,
                                                                    __nv_bfloat16* packed,
                                                                    float* partials) {
-  const long long chunk = blockIdx.x;
+  const long long chunk = base + blockIdx.x;
   const EwMat& E = ew[find_mat<false>(ew, n, chunk)];
   const long long start = (chunk - E.chunk_begin) * kChunk;
   const long long end = min(E.numel, start + kChunk);
@@ -147,10 +150,10 @@ __global__ void __launch_bounds__(kEwThreads) momentum_pack_kernel(const EwMat* 
 }
 
 __global__ void __launch_bounds__(kEwThreads) norm_partials_kernel(const EwMat* __restrict__ ew,
-                                                                   int n,
+                                                                   int n, long long base,
                                                                    const __nv_bfloat16* packed,
                                                                    float* partials) {
-  const long long chunk = blockIdx.x;
+  const long long chunk = base + blockIdx.x;
   const EwMat& E = ew[find_mat<false>(ew, n, chunk)];
   const long long start = (chunk - E.chunk_begin) * kChunk;
   const long long end = min(E.numel, start + kChunk);
@@ -195,10 +198,11 @@ __global__ void __launch_bounds__(kEwThreads) norm_finalize_kernel(const EwMat* 
 }
 
 __global__ void __launch_bounds__(kEwThreads) relayout_kernel(const EwMat* __restrict__ ew, int n,
+                                                              long long base,
                                                               const __nv_bfloat16* packed,
                                                               const float* inv_norm) {
   __shared__ float tile[kRelayTile][kRelayTile + 1];
-  const long long t = blockIdx.x;
+  const long long t = base + blockIdx.x;
   const int i = find_mat<true>(ew, n, t);
   const EwMat& E = ew[i];
   const long long local = t - E.tile_begin;
@@ -265,9 +269,10 @@ __global__ void __launch_bounds__(kEwThreads) relayout_kernel(const EwMat* __res
 }
 
 __global__ void __launch_bounds__(kEwThreads) scale_inplace_kernel(const EwMat* __restrict__ ew,
-                                                                   int n, __nv_bfloat16* packed,
+                                                                   int n, long long base,
+                                                                   __nv_bfloat16* packed,
                                                                    const float* inv_norm) {
-  const long long chunk = blockIdx.x;
+  const long long chunk = base + blockIdx.x;
   const int i = find_mat<false>(ew, n, chunk);
   const EwMat& E = ew[i];
   const long long start = (chunk - E.chunk_begin) * kChunk;
@@ -293,9 +298,9 @@ __global__ void __launch_bounds__(kEwThreads) scale_inplace_kernel(const EwMat* 
 
 template <bool W_BF16>
 __global__ void __launch_bounds__(kEwThreads) update_kernel(const EwMat* __restrict__ ew, int n,
-                                                            float lr,
+                                                            long long base, float lr,
                                                             const __nv_bfloat16* packed) {
-  const long long chunk = blockIdx.x;
+  const long long chunk = base + blockIdx.x;
   const EwMat& E = ew[find_mat<false>(ew, n, chunk)];
   const long long start = (chunk - E.chunk_begin) * kChunk;
   const long long end = min(E.numel, start + kChunk);
@@ -477,54 +482,58 @@ cudaError_t launch_upload(void* dst, const void* src, size_t bytes, cudaStream_t
   return cudaSuccess;
 }
 
-cudaError_t launch_momentum_pack(const EwMat* ew, int n, long long total_chunks, bool grad_bf16,
-                                 float beta, __nv_bfloat16* packed, float* partials,
-                                 cudaStream_t s) {
-  if (total_chunks <= 0) return cudaSuccess;
+cudaError_t launch_momentum_pack(const EwRange& r, bool grad_bf16, float beta,
+                                 __nv_bfloat16* packed, float* partials, cudaStream_t s) {
+  if (r.chunks <= 0) return cudaSuccess;
   if (grad_bf16)
-    momentum_pack_kernel<true><<<grid_of(total_chunks), kEwThreads, 0, s>>>(ew, n, beta, packed,
-                                                                            partials);
+    momentum_pack_kernel<true><<<grid_of(r.chunks), kEwThreads, 0, s>>>(r.ew, r.n, r.chunk_base,
+                                                                        beta, packed, partials);
   else
-    momentum_pack_kernel<false><<<grid_of(total_chunks), kEwThreads, 0, s>>>(ew, n, beta, packed,
-                                                                             partials);
+    momentum_pack_kernel<false><<<grid_of(r.chunks), kEwThreads, 0, s>>>(r.ew, r.n, r.chunk_base,
+                                                                         beta, packed, partials);
   return counted(cudaGetLastError());
 }
 
-cudaError_t launch_norm_partials(const EwMat* ew, int n, long long total_chunks,
-                                 const __nv_bfloat16* packed, float* partials, cudaStream_t s) {
-  if (total_chunks <= 0) return cudaSuccess;
-  norm_partials_kernel<<<grid_of(total_chunks), kEwThreads, 0, s>>>(ew, n, packed, partials);
+cudaError_t launch_norm_partials(const EwRange& r, const __nv_bfloat16* packed, float* partials,
+                                 cudaStream_t s) {
+  if (r.chunks <= 0) return cudaSuccess;
+  norm_partials_kernel<<<grid_of(r.chunks), kEwThreads, 0, s>>>(r.ew, r.n, r.chunk_base, packed,
+                                                                partials);
   return counted(cudaGetLastError());
 }
 
-cudaError_t launch_norm_finalize(const EwMat* ew, int n, const float* partials, float eps,
+cudaError_t launch_norm_finalize(const EwRange& r, const float* partials, float eps,
                                  float* inv_norm, cudaStream_t s) {
-  if (n <= 0) return cudaSuccess;
-  norm_finalize_kernel<<<n, kEwThreads, 0, s>>>(ew, partials, eps, inv_norm);
+  if (r.n <= 0) return cudaSuccess;
+  norm_finalize_kernel<<<r.n, kEwThreads, 0, s>>>(r.ew, partials, eps, inv_norm + r.first);
   return counted(cudaGetLastError());
 }
 
-cudaError_t launch_relayout(const EwMat* ew, int n, long long total_tiles,
-                            const __nv_bfloat16* packed, const float* inv_norm, cudaStream_t s) {
-  if (total_tiles <= 0) return cudaSuccess;
-  relayout_kernel<<<grid_of(total_tiles), kEwThreads, 0, s>>>(ew, n, packed, inv_norm);
+cudaError_t launch_relayout(const EwRange& r, const __nv_bfloat16* packed, const float* inv_norm,
+                            cudaStream_t s) {
+  if (r.tiles <= 0) return cudaSuccess;
+  relayout_kernel<<<grid_of(r.tiles), kEwThreads, 0, s>>>(r.ew, r.n, r.tile_base, packed,
+                                                          inv_norm + r.first);
   return counted(cudaGetLastError());
 }
 
-cudaError_t launch_scale_inplace(const EwMat* ew, int n, long long total_chunks,
-                                 __nv_bfloat16* packed, const float* inv_norm, cudaStream_t s) {
-  if (total_chunks <= 0) return cudaSuccess;
-  scale_inplace_kernel<<<grid_of(total_chunks), kEwThreads, 0, s>>>(ew, n, packed, inv_norm);
+cudaError_t launch_scale_inplace(const EwRange& r, __nv_bfloat16* packed, const float* inv_norm,
+                                 cudaStream_t s) {
+  if (r.chunks <= 0) return cudaSuccess;
+  scale_inplace_kernel<<<grid_of(r.chunks), kEwThreads, 0, s>>>(r.ew, r.n, r.chunk_base, packed,
+                                                                inv_norm + r.first);
   return counted(cudaGetLastError());
 }
 
-cudaError_t launch_update(const EwMat* ew, int n, long long total_chunks, bool weight_bf16,
-                          float lr, const __nv_bfloat16* packed, cudaStream_t s) {
-  if (total_chunks <= 0) return cudaSuccess;
+cudaError_t launch_update(const EwRange& r, bool weight_bf16, float lr,
+                          const __nv_bfloat16* packed, cudaStream_t s) {
+  if (r.chunks <= 0) return cudaSuccess;
   if (weight_bf16)
-    update_kernel<true><<<grid_of(total_chunks), kEwThreads, 0, s>>>(ew, n, lr, packed);
+    update_kernel<true><<<grid_of(r.chunks), kEwThreads, 0, s>>>(r.ew, r.n, r.chunk_base, lr,
+                                                                 packed);
   else
-    update_kernel<false><<<grid_of(total_chunks), kEwThreads, 0, s>>>(ew, n, lr, packed);
+    update_kernel<false><<<grid_of(r.chunks), kEwThreads, 0, s>>>(r.ew, r.n, r.chunk_base, lr,
+                                                                  packed);
   return counted(cudaGetLastError());
 }
 

@@ -30,19 +30,27 @@ cudaError_t launch_diag_shift(const Bucket* buckets, int n_buckets, int first_in
 // Copy `bytes` (multiple of 16) from host memory into device memory through
 // kernel parameters (stream-ordered, no host staging, no allocation).
 cudaError_t launch_upload(void* dst, const void* src, size_t bytes, cudaStream_t s);
-cudaError_t launch_momentum_pack(const EwMat* ew, int n, long long total_chunks, bool grad_bf16,
-                                 float beta, __nv_bfloat16* packed, float* partials,
+// A contiguous range of the per-matrix table: ew[0, n) are entries first ..
+// first + n - 1 (device pointer to entry `first`); their elementwise chunks are
+// [chunk_base, chunk_base + chunks) and their relayout tiles
+// [tile_base, tile_base + tiles).
+struct EwRange {
+  const EwMat* ew;
+  int n, first;
+  long long chunk_base, chunks, tile_base, tiles;
+};
+cudaError_t launch_momentum_pack(const EwRange& r, bool grad_bf16, float beta,
+                                 __nv_bfloat16* packed, float* partials, cudaStream_t s);
+cudaError_t launch_norm_partials(const EwRange& r, const __nv_bfloat16* packed, float* partials,
                                  cudaStream_t s);
-cudaError_t launch_norm_partials(const EwMat* ew, int n, long long total_chunks,
-                                 const __nv_bfloat16* packed, float* partials, cudaStream_t s);
-cudaError_t launch_norm_finalize(const EwMat* ew, int n, const float* partials, float eps,
+cudaError_t launch_norm_finalize(const EwRange& r, const float* partials, float eps,
                                  float* inv_norm, cudaStream_t s);
-cudaError_t launch_relayout(const EwMat* ew, int n, long long total_tiles,
-                            const __nv_bfloat16* packed, const float* inv_norm, cudaStream_t s);
-cudaError_t launch_scale_inplace(const EwMat* ew, int n, long long total_chunks,
-                                 __nv_bfloat16* packed, const float* inv_norm, cudaStream_t s);
-cudaError_t launch_update(const EwMat* ew, int n, long long total_chunks, bool weight_bf16,
-                          float lr, const __nv_bfloat16* packed, cudaStream_t s);
+cudaError_t launch_relayout(const EwRange& r, const __nv_bfloat16* packed, const float* inv_norm,
+                            cudaStream_t s);
+cudaError_t launch_scale_inplace(const EwRange& r, __nv_bfloat16* packed, const float* inv_norm,
+                                 cudaStream_t s);
+cudaError_t launch_update(const EwRange& r, bool weight_bf16, float lr,
+                          const __nv_bfloat16* packed, cudaStream_t s);
 cudaError_t launch_wait_timeout(int* err, long long budget_cycles, cudaStream_t s);
 cudaError_t launch_adamw(const AdamTensor* ts, int n, long long total_chunks, bool p_bf16,
                          bool g_bf16, const AdamScalars& k, cudaStream_t s);

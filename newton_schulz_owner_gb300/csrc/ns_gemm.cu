@@ -147,7 +147,7 @@ DM_DEV void producer(const GemmArgs& g, uint32_t rank, uint8_t* sA, uint8_t* sB,
   uint32_t phase = 0;
   int prev_bucket = -1;
   for (int t = int(cluster_id_x()); t < g.total_tiles; t += clusters) {
-    const TileInfo T = decode_tile<FULL>(g, t);
+    const TileInfo T = decode_tile<FULL>(g, g.tile_base + t);
     const Bucket& B = g.buckets[T.bucket];
     const void* mapL = tmap_of(g, B, g.sL);
     const void* mapR = tmap_of(g, B, g.sR);
@@ -197,7 +197,7 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
   uint32_t phase = 0;
   int it = 0;
   for (int t = int(cluster_id_x()); t < g.total_tiles; t += clusters, ++it) {
-    const TileInfo T = decode_tile<FULL>(g, t);
+    const TileInfo T = decode_tile<FULL>(g, g.tile_base + t);
     const Bucket& B = g.buckets[T.bucket];
     const int KB = (k_extent<FULL>(g, B) + kBK - 1) / kBK;
     const int acc = it & 1;
@@ -336,7 +336,7 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
   const int clusters = int(cluster_count_x());
   int it = 0;
   for (int t = int(cluster_id_x()); t < g.total_tiles; t += clusters, ++it) {
-    const TileInfo T = decode_tile<FULL>(g, t);
+    const TileInfo T = decode_tile<FULL>(g, g.tile_base + t);
     const Bucket& B = g.buckets[T.bucket];
     const int acc = it & 1;
     const uint32_t aph = uint32_t(it >> 1) & 1u;

@@ -108,6 +108,7 @@ struct GemmArgs {
   int* err;
   int n_buckets;
   int total_tiles;
+  int tile_base;                 // tile index of the launch's first tile (buckets[0]'s prefix)
   int sL, sR, sAux, sOut;
   const float* shift;            // per-matrix diagonal shift, or null
   int final_out;                 // full product: write O into `packed`
