@@ -61,6 +61,34 @@ def test_resume_from_saved_state_is_bit_identical(dm):
     assert not _same(W3, W2)          # the third step did change the weights
 
 
+def test_overlapped_step_equals_three_separate_calls(dm):
+    """dmuon_muon_step runs the memory-bound kernels of one bucket group on a
+    second stream next to the other group's products; the result must be the
+    same bits as pack, Newton-Schulz and update called one after another."""
+    from newton_schulz_owner_gb300 import workloads as wl
+    outs = []
+    for mode in ("whole", "three"):
+        own = dm.MuonOwner(SHAPES)
+        W = [wl.random_matrix(s, 700 + i, "cuda", 0.02, torch.bfloat16) for i, s in enumerate(SHAPES)]
+        M = [torch.zeros(s, device="cuda") for s in SHAPES]
+        for k in range(2):
+            G = [wl.random_matrix(s, 10_000 * (k + 1) + i, "cuda", 1e-3, torch.bfloat16)
+                 for i, s in enumerate(SHAPES)]
+            if mode == "whole":
+                own.step(G, M, W, lr=0.02, beta=0.95, ns_steps=5)
+            else:
+                dm.pack(SHAPES, G, M, 0.95, own.packed, own.offsets, own.workspace)
+                dm.ns_batched(SHAPES, own.packed, own.offsets, own.workspace, ns_steps=5,
+                              use_pack_norms=True)
+                dm.unpack_update(SHAPES, W, 0.02, own.packed, own.offsets, own.workspace)
+            assert own.status() == dm.OK
+        torch.cuda.synchronize()
+        outs.append(([w.cpu() for w in W], [m.cpu() for m in M],
+                     [own.packed_view(i).cpu() for i in range(len(SHAPES))]))
+    for a, b in zip(outs[0], outs[1]):
+        assert _same(a, b)
+
+
 def test_two_runs_are_bit_identical(dm):
     from newton_schulz_owner_gb300 import workloads as wl
     a = _run(dm, wl, 2)
