@@ -211,7 +211,7 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
   P.off_sym = off;
   off = align_up(off + size_t(P.sym_total) * sizeof(int), 128);
   P.off_tmaps = off;
-  off = align_up(off + P.buckets.size() * kSlots * 128, 16);
+  off = align_up(off + P.buckets.size() * kMapsPerBucket * 128, 16);
   P.tables_bytes = off - P.off_tables;
   off = align_up(off, 256);
   P.off_partials = off;
@@ -292,16 +292,23 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// One 3-D map (cols, rows, matrix) over a slot.  Operand maps move 64 x 64
+// boxes with the 128-byte swizzle that the MMA descriptors expect; epilogue
+// maps move the 32 x 32 chunks of one epilogue warp with the 64-byte swizzle
+// (one 64-byte row per chunk row).  Reads outside (cols, rows) are zero-filled
+// and writes outside are dropped, which handles ragged edges.
 bool encode_slot_map(CUtensorMap* map, void* base, int cols, int rows, int count, int pitch,
-                     long long stride) {
+                     long long stride, bool epilogue) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {cuuint64_t(cols), cuuint64_t(rows), cuuint64_t(count)};
   const cuuint64_t strides[2] = {cuuint64_t(pitch) * 2, cuuint64_t(stride) * 2};
-  const cuuint32_t box[3] = {64, 64, 1};
+  const cuuint32_t box_op[3] = {64, 64, 1};
+  const cuuint32_t box_epi[3] = {32, 32, 1};
   const cuuint32_t es[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides,
+             epilogue ? box_epi : box_op, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             epilogue ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -424,15 +431,17 @@ int upload_tables(const Request& R, const Plan& P) {
     B.pitch_m = BP.pitch_m;
     B.stride_x = BP.stride_x;
     B.stride_m = BP.stride_m;
-    B.tmap = int(b) * kSlots;
+    B.tmap = int(b) * kMapsPerBucket;
     for (int s = 0; s < kSlots; ++s) {
       if (!BP.used[s] || !R.do_ns) continue;
       void* base = ws + BP.slot_off[s];
       B.slot[s] = static_cast<__nv_bfloat16*>(base);
       const bool x = slot_is_x(s);
-      if (!encode_slot_map(&maps[b * kSlots + s], base, x ? BP.n : BP.m, BP.m, B.count,
-                           x ? BP.pitch_x : BP.pitch_m, x ? BP.stride_x : BP.stride_m))
-        return DMUON_ERR_CUDA;
+      for (int epi = 0; epi < 2; ++epi)
+        if (!encode_slot_map(&maps[b * kMapsPerBucket + epi * kSlots + s], base,
+                             x ? BP.n : BP.m, BP.m, B.count, x ? BP.pitch_x : BP.pitch_m,
+                             x ? BP.stride_x : BP.stride_m, epi != 0))
+          return DMUON_ERR_CUDA;
     }
     B.sym_off = sym_off;
     B.sym_count = int(BP.sym.size());

@@ -23,8 +23,9 @@
 //               the pair; in the leader, lane 0 issues the MMAs and commits
 //               to the barriers of both CTAs
 //   warps 2-9   epilogue (both CTAs): tcgen05.ld of this CTA's 128 rows, fused
-//               polynomial / axpy, bf16 stores, then release the accumulator
-//               to the leader
+//               polynomial / axpy, bf16 chunks staged in shared memory and
+//               written by TMA tensor stores (the a*X operand also arrives by
+//               TMA), then release the accumulator to the leader
 // Pair tiles are handed out statically (tile = cluster + k * clusters), so all
 // roles of both CTAs walk the same sequence without talking to each other.
 #include "dmuon.h"
@@ -47,8 +48,13 @@ constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
-constexpr int kBarBytes = 256;
-constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 + kBarBytes;
+constexpr int kEpiBufBytes = 32 * 32 * 2;              // one 32 x 32 bf16 epilogue chunk
+constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;  // two chunk buffers per epilogue warp
+constexpr int kBarBytes = 512;
+constexpr size_t kSmemBytes =
+    size_t(kStages) * kStageBytes + kEpiBytes + 1024 + kBarBytes;
+static_assert(kSmemBytes <= 232448, "dynamic shared memory above the sm_100 per-block limit");
+static_assert((2 * kStages + 5 + 2 * kEpiWarps) * 8 + 8 <= kBarBytes, "barrier area too small");
 // After a bounded wait gives up, wait this long before leaving so that copies
 // and MMAs already issued to this CTA's shared memory / TMEM have landed.
 constexpr long long kAbortSettleCycles = 400000;
@@ -243,129 +249,258 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
   (void)mbar_wait(drain_bar, 0, nullptr);
 }
 
-template <bool FULL>
-DM_DEV void store_tile_chunk(const GemmArgs& g, const Bucket& B, const TileInfo& T, int r,
-                             int c0, float alpha, const float (&acc)[32]) {
-  float o[32];
-  if (!FULL) {
-    const int m = B.m;
-    const int pm = B.pitch_m;
-    __nv_bfloat16* out = B.slot[g.sOut] + (long long)T.mat * B.stride_m;
-    if (g.beta != 0.f) {
-      float a[32];
-      load_bf16x32(B.slot[g.sAux] + (long long)T.mat * B.stride_m + (long long)r * pm + c0, a);
+// ------------------------------------------------------------------ epilogue
+// Each epilogue warp moves its 32 accumulator rows in chunks of 32 columns.
+// A chunk goes through one of the warp's two 2 KB shared-memory buffers, laid
+// out as the TMA 64-byte swizzle expects (16-byte unit u of row i at byte
+// i*64 + ((u ^ ((i >> 1) & 3)) << 4)): each thread writes its whole row there
+// without bank conflicts, and one lane stores the chunk to global memory with
+// a TMA tensor store.  The a*X operand of B*X arrives the same way, by TMA
+// loads issued ahead of time into the chunk's buffer.
+DM_DEV uint32_t epi_off(int row, int unit) {
+  return uint32_t(row * 64 + ((unit ^ ((row >> 1) & 3)) << 4));
+}
+
+DM_DEV void epi_store_row(uint32_t buf, int row, const float (&o)[32]) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = fmaf(g.gamma, acc[j], g.beta * a[j]);
-    } else {
+  for (int u = 0; u < 4; ++u)
+    st_shared_v4(buf + epi_off(row, u), pack_bf16x2(o[8 * u], o[8 * u + 1]),
+                 pack_bf16x2(o[8 * u + 2], o[8 * u + 3]), pack_bf16x2(o[8 * u + 4], o[8 * u + 5]),
+                 pack_bf16x2(o[8 * u + 6], o[8 * u + 7]));
+}
+
+DM_DEV void epi_load_row(uint32_t buf, int row, float (&x)[32]) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = g.gamma * acc[j];
+  for (int u = 0; u < 4; ++u) {
+    uint32_t w[4];
+    ld_shared_v4(buf + epi_off(row, u), w[0], w[1], w[2], w[3]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+      x[8 * u + 2 * k] = f.x;
+      x[8 * u + 2 * k + 1] = f.y;
     }
-    if (alpha != 0.f) {
-      const int d = r - c0;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j == d) o[j] += alpha;
-    }
-    __nv_bfloat16* row = out + (long long)r * pm;
-    if (c0 >= r && c0 + 32 <= m) {
+  }
+}
+
+// Element (row, col) of a chunk buffer.
+DM_DEV void epi_store_elem(uint32_t buf, int row, int col, float v) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(v);
+  st_shared_b16(buf + epi_off(row, col >> 3) + uint32_t((col & 7) * 2),
+                *reinterpret_cast<const uint16_t*>(&b));
+}
+
+DM_DEV const void* emap_of(const GemmArgs& g, const Bucket& B, int slot) {
+  return g.tmaps + size_t(B.tmap + kSlots + slot) * 128;
+}
+
+// Last product of a Newton-Schulz run: O goes straight into the packed buffer
+// in the parameter's orientation (row r of the working matrix, columns
+// c0..c0+31).
+DM_DEV void store_final_chunk(const GemmArgs& g, const Bucket& B, const TileInfo& T, int r,
+                              int c0, const float (&o)[32]) {
+  const int m = B.m, n = B.n;
+  const InternalMat im = g.imat[B.first + T.mat];
+  __nv_bfloat16* P = g.packed + im.packed_off;
+  if (!im.transposed) {
+    __nv_bfloat16* row = P + (long long)r * n;
+    if ((n & 7) == 0 && c0 + 32 <= n) {
       store_bf16x32(row + c0, o);
     } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int col = c0 + j;
-        if (col >= r && col < m) row[col] = __float2bfloat16_rn(o[j]);
-      }
-    }
-    // mirror: lanes hold consecutive rows, so each store is one 64-byte run
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int col = c0 + j;
-      if (col > r && col < m) out[(long long)col * pm + r] = __float2bfloat16_rn(o[j]);
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < n) row[c0 + j] = __float2bfloat16_rn(o[j]);
     }
   } else {
-    const int m = B.m, n = B.n;
-    if (alpha != 0.f || g.shift != nullptr) {
-      float x[32];
-      load_bf16x32(B.slot[g.sAux] + (long long)T.mat * B.stride_x + (long long)r * B.pitch_x + c0,
-                   x);
+    // parameter is (n, m): element (r, c) of X goes to row c, column r
 #pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = fmaf(g.gamma, acc[j], alpha * x[j]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = g.gamma * acc[j];
-    }
-    if (!g.final_out) {
-      __nv_bfloat16* row =
-          B.slot[g.sOut] + (long long)T.mat * B.stride_x + (long long)r * B.pitch_x;
-      if (c0 + 32 <= n) {
-        store_bf16x32(row + c0, o);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c0 + j < n) row[c0 + j] = __float2bfloat16_rn(o[j]);
-      }
-    } else {
-      const InternalMat im = g.imat[B.first + T.mat];
-      __nv_bfloat16* P = g.packed + im.packed_off;
-      if (!im.transposed) {
-        __nv_bfloat16* row = P + (long long)r * n;
-        if ((n & 7) == 0 && c0 + 32 <= n) {
-          store_bf16x32(row + c0, o);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c0 + j < n) row[c0 + j] = __float2bfloat16_rn(o[j]);
-        }
-      } else {
-        // parameter is (n, m): element (r, c) of X goes to row c, column r
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c0 + j < n) P[(long long)(c0 + j) * m + r] = __float2bfloat16_rn(o[j]);
-      }
-    }
+    for (int j = 0; j < 32; ++j)
+      if (c0 + j < n) P[(long long)(c0 + j) * m + r] = __float2bfloat16_rn(o[j]);
   }
 }
 
 template <bool FULL>
 DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t* tempty,
-                     uint32_t tmem_base, volatile int* abort_flag) {
+                     uint64_t* aux_bar_all, uint32_t epi_smem, uint32_t tmem_base,
+                     volatile int* abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;          // TMEM lane quarter this warp may read
   const int h = (warp - 2) >> 2;   // which 128-column half of the tile
+  const int ew = warp - 2;         // epilogue warp 0..7
+  const uint32_t buf0 = epi_smem + uint32_t(ew * 2 * kEpiBufBytes);
+  auto buf = [buf0](int b) { return buf0 + uint32_t(b * kEpiBufBytes); };
+  uint64_t* aux_bar = aux_bar_all + 2 * ew;
+  uint32_t aux_parity = 0;         // bit b: parity of the next completion of aux_bar[b]
   const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
   const int clusters = int(cluster_count_x());
-  int it = 0;
-  for (int t = int(cluster_id_x()); t < g.total_tiles; t += clusters, ++it) {
+  const int r_loc = int(rank) * kCtaM + q * 32;  // first tile row of this warp's chunks
+  // a*X of B*X (also in the final product) comes in by TMA
+  const bool aux_tma = FULL && (g.alpha != 0.f || g.shift != nullptr);
+  int acq_bucket = -1;
+
+  // lane 0: order the map writes before the TMA unit reads this bucket's maps
+  auto acquire_maps = [&](int bucket, const Bucket& B) {
+    if (bucket == acq_bucket) return;
+    tensormap_acquire(emap_of(g, B, g.sOut));
+    if (aux_tma) tensormap_acquire(emap_of(g, B, g.sAux));
+    acq_bucket = bucket;
+  };
+  // lane 0: TMA load of chunk cc of tile T's a*X operand into buffer cc & 1
+  auto issue_aux = [&](const TileInfo& T, const Bucket& B, int cc) {
+    const int c0 = T.tj * kTileN + h * 128 + cc * 32;
+    if (c0 >= B.n) return;
+    const int b = cc & 1;
+    mbar_arrive_expect_tx(&aux_bar[b], kEpiBufBytes);
+    tma_load_3d_u32(buf(b), emap_of(g, B, g.sAux), smem_u32(&aux_bar[b]), c0,
+                    T.ti * kTileM + r_loc, T.mat);
+  };
+
+  int t = int(cluster_id_x());
+  if (aux_tma && t < g.total_tiles && lane == 0) {
     const TileInfo T = decode_tile<FULL>(g, g.tile_base + t);
     const Bucket& B = g.buckets[T.bucket];
+    acquire_maps(T.bucket, B);
+    issue_aux(T, B, 0);
+    issue_aux(T, B, 1);
+  }
+  bool ok = true;
+  int it = 0;
+  for (; ok && t < g.total_tiles; t += clusters, ++it) {
+    const TileInfo T = decode_tile<FULL>(g, g.tile_base + t);
+    const Bucket& B = g.buckets[T.bucket];
+    if (lane == 0) acquire_maps(T.bucket, B);
     const int acc = it & 1;
     const uint32_t aph = uint32_t(it >> 1) & 1u;
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait_cluster(&tfull[acc], aph, abort_flag) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) {
+    int w = 1;
+    if (lane == 0) w = mbar_wait_cluster(&tfull[acc], aph, abort_flag) ? 1 : 0;
+    w = __shfl_sync(0xffffffffu, w, 0);
+    if (!w) {
       if (lane == 0) raise_abort(g.err, abort_flag);
       break;
     }
     tc_fence_after();
-    const int r = T.ti * kTileM + int(rank) * kCtaM + q * 32 + lane;
     const int ncols = FULL ? B.n : B.m;
+    const int rg0 = T.ti * kTileM + r_loc;  // first output row of this warp's chunks
+    const int r = rg0 + lane;
     const float alpha =
         g.shift != nullptr ? g.alpha + g.shift_sign * g.shift[B.first + T.mat] : g.alpha;
+    const bool diag_tile = !FULL && T.ti == T.tj;
+    const void* out_map = emap_of(g, B, g.sOut);
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {
-      const int tcol = h * 128 + cc * 32;
-      const int c0 = T.tj * kTileN + tcol;
+      const int c_loc = h * 128 + cc * 32;
+      const int c0 = T.tj * kTileN + c_loc;
       if (c0 >= ncols) break;  // warp-uniform
+      // lower chunks of a diagonal tile are written as mirrors of upper ones
+      if (diag_tile && c_loc < r_loc) continue;
       float v[32];
-      tmem_ld32(tmem_base + uint32_t(acc * kAccCols + tcol) + (uint32_t(q * 32) << 16), v);
+      tmem_ld32(tmem_base + uint32_t(acc * kAccCols + c_loc) + (uint32_t(q * 32) << 16), v);
       tmem_ld_wait();
-      if (r < B.m) store_tile_chunk<FULL>(g, B, T, r, c0, alpha, v);
+      float o[32];
+      if constexpr (FULL) {
+        const int b = cc & 1;
+        if (aux_tma) {
+          int wa = 1;
+          if (lane == 0) wa = mbar_wait(&aux_bar[b], (aux_parity >> b) & 1u, abort_flag) ? 1 : 0;
+          wa = __shfl_sync(0xffffffffu, wa, 0);
+          aux_parity ^= 1u << b;
+          if (!wa) {
+            if (lane == 0) raise_abort(g.err, abort_flag);
+            ok = false;
+            break;
+          }
+          float x[32];
+          epi_load_row(buf(b), lane, x);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = fmaf(g.gamma, v[j], alpha * x[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = g.gamma * v[j];
+          // nothing was loaded into this buffer: wait until no store reads it
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+        }
+        if (!g.final_out) {
+          epi_store_row(buf(b), lane, o);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(out_map, buf(b), c0, rg0, T.mat);
+            bulk_commit();
+          }
+        } else {
+          if (r < B.m) store_final_chunk(g, B, T, r, c0, o);
+          __syncwarp();  // every lane is done reading buffer b
+        }
+        // operand of chunk cc + 2 into the buffer just used
+        if (aux_tma && cc + 2 < 4 && lane == 0) {
+          if (!g.final_out) bulk_wait_read<0>();
+          issue_aux(T, B, cc + 2);
+        }
+      } else {
+        const int m = B.m;
+        if (g.beta != 0.f) {
+          float a[32];
+          if (r < m) {
+            load_bf16x32(B.slot[g.sAux] + (long long)T.mat * B.stride_m +
+                             (long long)r * B.pitch_m + c0,
+                         a);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] = 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = fmaf(g.gamma, v[j], g.beta * a[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = g.gamma * v[j];
+        }
+        if (alpha != 0.f) {
+          const int d = r - c0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == d) o[j] += alpha;
+        }
+        // both buffers free of earlier stores
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        const bool diag_chunk = diag_tile && c_loc == r_loc;
+        epi_store_row(buf(0), lane, o);
+        if (diag_chunk) {
+          // lower triangle of the chunk := transpose of its upper triangle
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j > lane) epi_store_elem(buf(0), j, lane, o[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) epi_store_elem(buf(1), j, lane, o[j]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(out_map, buf(0), c0, rg0, T.mat);
+          if (!diag_chunk) tma_store_3d(out_map, buf(1), rg0, c0, T.mat);
+          bulk_commit();
+        }
+      }
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive_cluster(leader_tempty + uint32_t(acc) * 8u);
+    // operands of the next tile's first two chunks
+    if (ok && aux_tma && lane == 0 && t + clusters < g.total_tiles) {
+      const TileInfo Tn = decode_tile<FULL>(g, g.tile_base + t + clusters);
+      const Bucket& Bn = g.buckets[Tn.bucket];
+      acquire_maps(Tn.bucket, Bn);
+      if (!g.final_out) bulk_wait_read<0>();
+      issue_aux(Tn, Bn, 0);
+      issue_aux(Tn, Bn, 1);
+    }
   }
+  // stores complete, and stop reading shared memory, before the CTA exits
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
 }
 
 template <bool FULL>
@@ -375,12 +510,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
                                              ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kAStage;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sB + kStages * kBStage);
+  uint8_t* sE = sB + kStages * kBStage;  // epilogue chunk buffers (1024-byte aligned)
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sE + kEpiBytes);
   uint64_t* empty_bar = full_bar + kStages;
   uint64_t* tfull = empty_bar + kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain_bar = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint64_t* aux_bar = drain_bar + 1;     // two per epilogue warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + 2 * kEpiWarps);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -395,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       mbar_init(&tempty[a], 2 * kEpiWarps);  // leader: every epilogue warp of both CTAs
     }
     mbar_init(drain_bar, 1);
+    for (int a = 0; a < 2 * kEpiWarps; ++a) mbar_init(&aux_bar[a], 1);  // lane 0's expect_tx
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -414,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       mma_issuer<FULL>(g, sA, sB, full_bar, empty_bar, tfull, tempty, drain_bar, tmem_base,
                        abort_flag);
   } else if (warp >= 2) {
-    epilogue<FULL>(g, rank, tfull, tempty, tmem_base, abort_flag);
+    epilogue<FULL>(g, rank, tfull, tempty, aux_bar, smem_u32(sE), tmem_base, abort_flag);
   }
 
   __syncthreads();

@@ -18,6 +18,10 @@ constexpr int kRelayTile = 64;
 constexpr int kSlots = 8;
 enum Slot : int { SX0 = 0, SX1 = 1, SM0 = 2, SM1 = 3, SM2 = 4, SM3 = 5, SM4 = 6, SM5 = 7 };
 __host__ __device__ constexpr bool slot_is_x(int s) { return s < 2; }
+// Two TMA tensor maps per slot: the operand map (64 x 64 boxes, 128-byte
+// swizzle) at `slot`, and the epilogue map (32 x 32 boxes, 64-byte swizzle)
+// at `kSlots + slot`.
+constexpr int kMapsPerBucket = 2 * kSlots;
 
 // EwMat::flags
 constexpr int kFlagVecGM = 1;      // grad, momentum 16-byte aligned
@@ -52,7 +56,7 @@ struct Bucket {
   int pitch_x, pitch_m;          // row pitch (elements) of X slots / m x m slots
   long long stride_x, stride_m;  // elements between consecutive matrices
   __nv_bfloat16* slot[kSlots];   // base of each slot (null if unused)
-  int tmap;                      // index of the bucket's first tensor map (kSlots maps)
+  int tmap;                      // index of the bucket's first tensor map (kMapsPerBucket maps)
   int sym_off, sym_count;        // upper-triangle tile list of an m x m product
   int full_ti, full_tj;          // tile grid of an m x n product
   int sym_begin;                 // first tile of this bucket in a symmetric launch
