@@ -32,6 +32,7 @@ long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 struct BucketPlan {
   int m = 0, n = 0;
   bool gram = false;
+  bool tall = false;      // rows > cols: X slots hold Y = X^T (n x m), the parameter's layout
   std::vector<int> mats;  // caller indices, in caller order
   int pitch_x = 0, pitch_m = 0;
   long long stride_x = 0, stride_m = 0;
@@ -90,12 +91,14 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
   P.tiles_r.assign(n, 0);
   P.tiles_c.assign(n, 0);
 
-  // buckets keyed by (gram, m, n); standard first, each group in first-seen
-  // order, except that the standard bucket with the most elements goes last
-  // (a whole step overlaps its memory-bound work with the others' products)
-  std::map<std::tuple<int, int, int>, int> key_to_b;
-  std::map<std::tuple<int, int, int>, long long> key_elems;
-  std::vector<std::tuple<int, int, int>> order;
+  // buckets keyed by (gram, m, n, tall); standard first, each group in
+  // first-seen order, except that the standard bucket with the most elements
+  // goes last (a whole step overlaps its memory-bound work with the others'
+  // products)
+  using Key = std::tuple<int, int, int, int>;
+  std::map<Key, int> key_to_b;
+  std::map<Key, long long> key_elems;
+  std::vector<Key> order;
   for (int i = 0; i < n; ++i) {
     if (!shape_ok(shp[i])) return DMUON_ERR_INVALID_ARG;
     const long long r = shp[i].rows, c = shp[i].cols;
@@ -104,15 +107,19 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
     P.tiles_c[i] = int(ceil_div(c, kRelayTile));
     if (r == 0 || c == 0) continue;
     const int m = int(std::min(r, c)), nn = int(std::max(r, c));
-    const auto key = std::make_tuple(uses_gram(variant, m, nn) ? 1 : 0, m, nn);
+    const Key key(uses_gram(variant, m, nn) ? 1 : 0, m, nn, r > c ? 1 : 0);
     if (!key_to_b.count(key)) {
       key_to_b[key] = -1;
       order.push_back(key);
     }
     key_elems[key] += r * c;
   }
-  std::stable_sort(order.begin(), order.end(),
-                   [](const auto& a, const auto& b) { return std::get<0>(a) < std::get<0>(b); });
+  // within each group, wide/square buckets before tall ones, so that every
+  // product launch splits into few runs of one orientation
+  std::stable_sort(order.begin(), order.end(), [](const Key& a, const Key& b) {
+    return std::make_pair(std::get<0>(a), std::get<3>(a)) <
+           std::make_pair(std::get<0>(b), std::get<3>(b));
+  });
   {
     int n_std = 0, big = -1;
     for (size_t b = 0; b < order.size(); ++b) {
@@ -128,6 +135,7 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
     bp.gram = std::get<0>(order[b]) != 0;
     bp.m = std::get<1>(order[b]);
     bp.n = std::get<2>(order[b]);
+    bp.tall = std::get<3>(order[b]) != 0;
     P.buckets.push_back(bp);
     if (!bp.gram) P.n_std = int(b) + 1;
   }
@@ -135,7 +143,7 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
     const long long r = shp[i].rows, c = shp[i].cols;
     if (r == 0 || c == 0) continue;
     const int m = int(std::min(r, c)), nn = int(std::max(r, c));
-    const int b = key_to_b[std::make_tuple(uses_gram(variant, m, nn) ? 1 : 0, m, nn)];
+    const int b = key_to_b[Key(uses_gram(variant, m, nn) ? 1 : 0, m, nn, r > c ? 1 : 0)];
     P.bucket_of[i] = b;
     P.idx_in_bucket[i] = int(P.buckets[b].mats.size());
     P.buckets[b].mats.push_back(i);
@@ -143,9 +151,11 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
   int internal = 0;
   for (auto& B : P.buckets) {
     for (int i : B.mats) P.internal_of[i] = internal++;
-    B.pitch_x = int(align_up(size_t(B.n), 64));
+    // X slots in the parameter's orientation: m x n, or n x m for a tall bucket
+    const int x_rows = B.tall ? B.n : B.m, x_cols = B.tall ? B.m : B.n;
+    B.pitch_x = int(align_up(size_t(x_cols), 64));
     B.pitch_m = int(align_up(size_t(B.m), 64));
-    B.stride_x = (long long)B.m * B.pitch_x;
+    B.stride_x = (long long)x_rows * B.pitch_x;
     B.stride_m = (long long)B.m * B.pitch_m;
     if (!B.gram) {
       B.used[SX0] = B.used[SX1] = B.used[SM0] = B.used[SM1] = true;
@@ -157,8 +167,9 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
     const int J = int(ceil_div(B.m, kTileM));
     for (int ti = 0; ti < J; ++ti)
       for (int tj = ti; tj < J; ++tj) B.sym.push_back((ti << 16) | tj);
-    B.full_ti = J;
-    B.full_tj = int(ceil_div(B.n, kTileN));
+    // tile grid of the m x n product's output (X' or Y')
+    B.full_ti = int(ceil_div(x_rows, kTileM));
+    B.full_tj = int(ceil_div(x_cols, kTileN));
     P.sym_total += int(B.sym.size());
   }
   P.n_internal = internal;
@@ -431,15 +442,17 @@ int upload_tables(const Request& R, const Plan& P) {
     B.pitch_m = BP.pitch_m;
     B.stride_x = BP.stride_x;
     B.stride_m = BP.stride_m;
+    B.tall = BP.tall ? 1 : 0;
     B.tmap = int(b) * kMapsPerBucket;
     for (int s = 0; s < kSlots; ++s) {
       if (!BP.used[s] || !R.do_ns) continue;
       void* base = ws + BP.slot_off[s];
       B.slot[s] = static_cast<__nv_bfloat16*>(base);
       const bool x = slot_is_x(s);
+      const int cols = x && !BP.tall ? BP.n : BP.m, rows = x && BP.tall ? BP.n : BP.m;
       for (int epi = 0; epi < 2; ++epi)
-        if (!encode_slot_map(&maps[b * kMapsPerBucket + epi * kSlots + s], base,
-                             x ? BP.n : BP.m, BP.m, B.count, x ? BP.pitch_x : BP.pitch_m,
+        if (!encode_slot_map(&maps[b * kMapsPerBucket + epi * kSlots + s], base, cols, rows,
+                             B.count, x ? BP.pitch_x : BP.pitch_m,
                              x ? BP.stride_x : BP.stride_m, epi != 0))
           return DMUON_ERR_CUDA;
     }
@@ -466,20 +479,10 @@ struct GemmLauncher {
   unsigned char* ws;
   int b0, b1;
   cudaStream_t stream;
-  int sym_tiles = 0, full_tiles = 0;
 
   GemmLauncher(const Plan& p, const Request& r, int c, unsigned char* w, int lo, int hi,
                cudaStream_t s)
-      : P(p), R(r), clusters(c), ws(w), b0(lo), b1(hi), stream(s) {
-    long long st = 0, ft = 0;
-    for (int b = b0; b < b1; ++b) {
-      const BucketPlan& B = P.buckets[b];
-      st += (long long)B.mats.size() * B.sym.size();
-      ft += (long long)B.mats.size() * B.full_ti * B.full_tj;
-    }
-    sym_tiles = int(st);
-    full_tiles = int(ft);
-  }
+      : P(p), R(r), clusters(c), ws(w), b0(lo), b1(hi), stream(s) {}
   GemmArgs base() const {
     GemmArgs g{};
     g.buckets = reinterpret_cast<const Bucket*>(ws + P.off_bk) + b0;
@@ -491,28 +494,54 @@ struct GemmLauncher {
     g.n_buckets = b1 - b0;
     return g;
   }
+  // One launch per run of consecutive buckets that need the same product kind
+  // (the planner keeps buckets of one orientation together within a group).
+  bool launch_runs(GemmArgs g, bool full, bool by_orientation) const {
+    int b = b0;
+    while (b < b1) {
+      const bool tall = P.buckets[b].tall;
+      int e = b + 1;
+      long long tiles = 0;
+      if (by_orientation)
+        while (e < b1 && P.buckets[e].tall == tall) ++e;
+      else
+        e = b1;
+      for (int k = b; k < e; ++k) {
+        const BucketPlan& B = P.buckets[k];
+        tiles += (long long)B.mats.size() * (full ? (long long)B.full_ti * B.full_tj
+                                                  : (long long)B.sym.size());
+      }
+      g.buckets = reinterpret_cast<const Bucket*>(ws + P.off_bk) + b;
+      g.n_buckets = e - b;
+      g.tile_base = full ? P.buckets[b].full_begin : P.buckets[b].sym_begin;
+      g.total_tiles = int(tiles);
+      const int kind = full ? (tall ? kFullTall : kFullWide)
+                            : (by_orientation && tall ? kSymMN : kSymK);
+      if (launch_ns_gemm(g, kind, clusters, stream) != cudaSuccess) return false;
+      b = e;
+    }
+    return true;
+  }
   // out = alpha*I + beta*aux + gamma*L R^T  (m x m, symmetric)
   bool sym(int sL, int sR, int sAux, int sOut, float alpha, float beta, float gamma,
            const float* shift = nullptr, float shift_sign = 0.f) const {
     GemmArgs g = base();
-    g.total_tiles = sym_tiles;
-    g.tile_base = P.buckets[b0].sym_begin;
     g.sL = sL; g.sR = sR; g.sAux = sAux; g.sOut = sOut;
     g.alpha = alpha; g.beta = beta; g.gamma = gamma;
     g.shift = shift; g.shift_sign = shift_sign;
-    return launch_ns_gemm(g, false, clusters, stream) == cudaSuccess;
+    // X X^T reads the X slots, whose layout follows the orientation
+    return launch_runs(g, false, slot_is_x(sL));
   }
-  // out = alpha*aux + gamma*L R  (m x n); final: write O into the packed buffer
+  // out = alpha*aux + gamma*L R  (m x n; Y' = alpha*Y + gamma*Y L for tall
+  // buckets); final: write O into the packed buffer
   bool full(int sL, int sR, int sAux, int sOut, float alpha, float gamma, bool final,
             const float* shift = nullptr, float shift_sign = 0.f) const {
     GemmArgs g = base();
-    g.total_tiles = full_tiles;
-    g.tile_base = P.buckets[b0].full_begin;
     g.sL = sL; g.sR = sR; g.sAux = sAux; g.sOut = sOut;
     g.alpha = alpha; g.beta = 0.f; g.gamma = gamma;
     g.shift = shift; g.shift_sign = shift_sign;
     g.final_out = final ? 1 : 0;
-    return launch_ns_gemm(g, true, clusters, stream) == cudaSuccess;
+    return launch_runs(g, true, true);
   }
   int first() const { return P.buckets[b0].first; }
   int n_mats() const {

@@ -4,8 +4,8 @@
 //                   packed <- bf16(U); per-chunk fp32 partial sums of U^2
 //   norm_partials   the same partial sums from bf16 values already packed
 //   norm_finalize   inv_i = 1 / (sqrt(sum of matrix i's partials) + eps), fp64
-//   relayout        X0 = U * inv into the working layout (transposed when
-//                   rows > cols), 64x64 tiles staged through shared memory
+//   relayout        X0 = U * inv into the working layout (the parameter's own
+//                   orientation, rows padded to the slot pitch)
 //   scale_inplace   packed <- bf16(U * inv)  (ns_steps = 0)
 //   update          W <- W - lr * sqrt(max(1, rows/cols)) * O
 // Every kernel reads and writes 16-byte vectors where the pointers allow and
@@ -197,74 +197,37 @@ __global__ void __launch_bounds__(kEwThreads) norm_finalize_kernel(const EwMat* 
   if (threadIdx.x == 0) inv_norm[blockIdx.x] = (float)(1.0 / (sqrt(red[0]) + (double)eps));
 }
 
+// X0 = U * inv into the working layout: the parameter's own orientation with
+// rows padded to the slot pitch.  One block per 64 x 64 tile of the parameter;
+// each thread copies 16 consecutive elements of one row.
 __global__ void __launch_bounds__(kEwThreads) relayout_kernel(const EwMat* __restrict__ ew, int n,
                                                               long long base,
                                                               const __nv_bfloat16* packed,
                                                               const float* inv_norm) {
-  __shared__ float tile[kRelayTile][kRelayTile + 1];
   const long long t = base + blockIdx.x;
   const int i = find_mat<true>(ew, n, t);
   const EwMat& E = ew[i];
   const long long local = t - E.tile_begin;
   const int tr = int(local / E.tiles_c), tc = int(local % E.tiles_c);
-  const int r0 = tr * kRelayTile, c0 = tc * kRelayTile;
-  const float inv = inv_norm[i];
-  const int lr = threadIdx.x >> 2, ls = (threadIdx.x & 3) * 16;
+  const int r = tr * kRelayTile + (threadIdx.x >> 2);
+  const int c0 = tc * kRelayTile + (threadIdx.x & 3) * 16;
   const int rows = E.rows, cols = E.cols;
-  {
-    const int r = r0 + lr;
-    if (r < rows) {
-      const __nv_bfloat16* src = packed + E.packed_off + (long long)r * cols + c0 + ls;
-      const int cnt = min(16, cols - (c0 + ls));
-      if (cnt == 16 && (E.flags & kFlagRowsAligned)) {
-        float f[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(src), f);
+  if (r >= rows || c0 >= cols) return;
+  const float inv = inv_norm[i];
+  const __nv_bfloat16* src = packed + E.packed_off + (long long)r * cols + c0;
+  __nv_bfloat16* dst = E.x0 + (long long)r * E.pitch_x + c0;
+  const int cnt = min(16, cols - c0);
+  if (cnt == 16 && (E.flags & kFlagRowsAligned)) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) tile[lr][ls + k] = f[k] * inv;
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + 8), f);
+    for (int v = 0; v < 2; ++v) {
+      float f[8];
+      bf16x8_to_f32(reinterpret_cast<const uint4*>(src)[v], f);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) tile[lr][ls + 8 + k] = f[k] * inv;
-      } else {
-        for (int k = 0; k < cnt; ++k) tile[lr][ls + k] = __bfloat162float(src[k]) * inv;
-      }
-    }
-  }
-  __syncthreads();
-  if (!E.transposed) {
-    const int r = r0 + lr;
-    if (r < rows) {
-      __nv_bfloat16* dst = E.x0 + (long long)r * E.pitch_x + c0 + ls;
-      const int cnt = min(16, cols - (c0 + ls));
-      if (cnt == 16) {
-        float f[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) f[k] = tile[lr][ls + k];
-        reinterpret_cast<uint4*>(dst)[0] = f32x8_to_bf16x8(f);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) f[k] = tile[lr][ls + 8 + k];
-        reinterpret_cast<uint4*>(dst)[1] = f32x8_to_bf16x8(f);
-      } else {
-        for (int k = 0; k < cnt; ++k) dst[k] = __float2bfloat16_rn(tile[lr][ls + k]);
-      }
+      for (int k = 0; k < 8; ++k) f[k] *= inv;
+      reinterpret_cast<uint4*>(dst)[v] = f32x8_to_bf16x8(f);
     }
   } else {
-    // working matrix is the transpose: its row (c0 + lr) holds parameter column c0 + lr
-    const int xr = c0 + lr;
-    if (xr < cols) {
-      __nv_bfloat16* dst = E.x0 + (long long)xr * E.pitch_x + r0 + ls;
-      const int cnt = min(16, rows - (r0 + ls));
-      if (cnt == 16) {
-        float f[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) f[k] = tile[ls + k][lr];
-        reinterpret_cast<uint4*>(dst)[0] = f32x8_to_bf16x8(f);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) f[k] = tile[ls + 8 + k][lr];
-        reinterpret_cast<uint4*>(dst)[1] = f32x8_to_bf16x8(f);
-      } else {
-        for (int k = 0; k < cnt; ++k) dst[k] = __float2bfloat16_rn(tile[ls + k][lr]);
-      }
-    }
+    for (int k = 0; k < cnt; ++k) dst[k] = __float2bfloat16_rn(__bfloat162float(src[k]) * inv);
   }
 }
 

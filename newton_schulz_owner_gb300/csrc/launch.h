@@ -20,7 +20,7 @@ size_t ns_gemm_smem_bytes();
 // Once per device: opt into large shared memory and find how many CTA pairs
 // (clusters of two) can be resident at once.
 cudaError_t ns_gemm_prepare(int num_sms, int* max_clusters);
-cudaError_t launch_ns_gemm(const GemmArgs& g, bool full, int max_clusters, cudaStream_t s);
+cudaError_t launch_ns_gemm(const GemmArgs& g, int kind, int max_clusters, cudaStream_t s);
 // Per-matrix diagonal shift b*s + c*s^2 with s = trace(A)/m, A = slot `slot`.
 cudaError_t launch_diag_shift(const Bucket* buckets, int n_buckets, int first_internal,
                               int n_mats, int slot, float b, float c, float* shift,

@@ -10,6 +10,11 @@
 // The standard Muon iteration is these three launches per step; the Gram
 // variant chains symmetric launches on m x m matrices.
 //
+// A tall parameter (rows > cols) keeps its own layout, Y = X^T (n x m), so no
+// matrix is ever transposed in memory: X X^T = Y^T Y reads both operands
+// MN-major from Y, and X' = a*X + B*X becomes Y' = a*Y + Y*B (B symmetric)
+// with both operands K-major.
+//
 // Work unit: a 256 x 256 output tile computed by a cluster of two CTAs on two
 // SMs with one tcgen05.mma.cta_group::2 (M=256, N=256, K=16).  Each CTA loads
 // only its 128 rows of L and its 128 columns of R per 64-wide K block (32 KB),
@@ -63,8 +68,21 @@ struct TileInfo {
   int bucket, mat, ti, tj;
 };
 
-template <bool FULL>
+template <int KIND>
+struct Kind {
+  static constexpr bool full = KIND == kFullWide || KIND == kFullTall;
+  static constexpr bool tall = KIND == kSymMN || KIND == kFullTall;
+  // operand majorness: K-major operands are loaded as 64 rows x 64 K-elements,
+  // MN-major ones as 64 K-rows x 64 contiguous M (or N) elements
+  static constexpr bool l_mn = KIND == kSymMN;
+  static constexpr bool r_mn = KIND == kSymMN || KIND == kFullWide;
+  // Y' = a Y + Y B: the X slot (named sR) is the left operand
+  static constexpr bool swap_lr = KIND == kFullTall;
+};
+
+template <int KIND>
 DM_DEV TileInfo decode_tile(const GemmArgs& g, int t) {
+  constexpr bool FULL = Kind<KIND>::full;
   int lo = 0, hi = g.n_buckets - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -76,13 +94,20 @@ DM_DEV TileInfo decode_tile(const GemmArgs& g, int t) {
   TileInfo T;
   T.bucket = lo;
   if (FULL) {
-    // column-panel major: consecutive tiles share the R (= X) column panel
+    // Consecutive tiles share the panel of the streamed m x n operand while
+    // the m x m operand stays in L2: column panels of X (wide: X' = a X + B X),
+    // row panels of Y (tall: Y' = a Y + Y B).
     const int local = t - B.full_begin;
     const int per = B.full_ti * B.full_tj;
     T.mat = local / per;
     const int r = local - T.mat * per;
-    T.tj = r / B.full_ti;
-    T.ti = r - T.tj * B.full_ti;
+    if (Kind<KIND>::tall) {
+      T.ti = r / B.full_tj;
+      T.tj = r - T.ti * B.full_tj;
+    } else {
+      T.tj = r / B.full_ti;
+      T.ti = r - T.tj * B.full_ti;
+    }
   } else {
     const int local = t - B.sym_begin;
     T.mat = local / B.sym_count;
@@ -94,9 +119,9 @@ DM_DEV TileInfo decode_tile(const GemmArgs& g, int t) {
   return T;
 }
 
-template <bool FULL>
+template <int KIND>
 DM_DEV int k_extent(const GemmArgs& g, const Bucket& B) {
-  if (FULL) return B.m;
+  if (Kind<KIND>::full) return B.m;
   return slot_is_x(g.sL) ? B.n : B.m;
 }
 
@@ -144,7 +169,7 @@ DM_DEV void store_bf16x32(__nv_bfloat16* p, const float (&f)[32]) {
 }
 
 // ------------------------------------------------------------------ roles
-template <bool FULL>
+template <int KIND>
 DM_DEV void producer(const GemmArgs& g, uint32_t rank, uint8_t* sA, uint8_t* sB,
                      uint64_t* full_bar, uint64_t* empty_bar, volatile int* abort_flag) {
   const uint32_t leader_full = mapa_shared(smem_u32(full_bar), 0);
@@ -153,16 +178,16 @@ DM_DEV void producer(const GemmArgs& g, uint32_t rank, uint8_t* sA, uint8_t* sB,
   uint32_t phase = 0;
   int prev_bucket = -1;
   for (int t = int(cluster_id_x()); t < g.total_tiles; t += clusters) {
-    const TileInfo T = decode_tile<FULL>(g, g.tile_base + t);
+    const TileInfo T = decode_tile<KIND>(g, g.tile_base + t);
     const Bucket& B = g.buckets[T.bucket];
-    const void* mapL = tmap_of(g, B, g.sL);
-    const void* mapR = tmap_of(g, B, g.sR);
+    const void* mapL = tmap_of(g, B, Kind<KIND>::swap_lr ? g.sR : g.sL);
+    const void* mapR = tmap_of(g, B, Kind<KIND>::swap_lr ? g.sL : g.sR);
     if (T.bucket != prev_bucket) {
       tensormap_acquire(mapL);
       tensormap_acquire(mapR);
       prev_bucket = T.bucket;
     }
-    const int KB = (k_extent<FULL>(g, B) + kBK - 1) / kBK;
+    const int KB = (k_extent<KIND>(g, B) + kBK - 1) / kBK;
     const int row0 = T.ti * kTileM + int(rank) * kCtaM;        // this CTA's rows of L
     const int col0 = T.tj * kTileN + int(rank) * (kTileN / 2);  // this CTA's columns of R
     for (int kb = 0; kb < KB; ++kb) {
@@ -175,12 +200,17 @@ DM_DEV void producer(const GemmArgs& g, uint32_t rank, uint8_t* sA, uint8_t* sB,
       uint8_t* b = sB + stage * kBStage;
       const uint32_t bar = leader_full + uint32_t(stage) * 8u;
       const int k0 = kb * kBK;
-      tma_load_3d_pair(a, mapL, bar, k0, row0, T.mat);
-      tma_load_3d_pair(a + kBox, mapL, bar, k0, row0 + 64, T.mat);
-      if (FULL) {  // R = X, MN-major: 64 K-rows x 64 columns per box
+      if (Kind<KIND>::l_mn) {  // 64 K-rows x 64 rows of L per box
+        tma_load_3d_pair(a, mapL, bar, row0, k0, T.mat);
+        tma_load_3d_pair(a + kBox, mapL, bar, row0 + 64, k0, T.mat);
+      } else {        // 64 rows of L x 64 K-elements per box
+        tma_load_3d_pair(a, mapL, bar, k0, row0, T.mat);
+        tma_load_3d_pair(a + kBox, mapL, bar, k0, row0 + 64, T.mat);
+      }
+      if (Kind<KIND>::r_mn) {
         tma_load_3d_pair(b, mapR, bar, col0, k0, T.mat);
         tma_load_3d_pair(b + kBox, mapR, bar, col0 + 64, k0, T.mat);
-      } else {     // R rows, K-major
+      } else {
         tma_load_3d_pair(b, mapR, bar, k0, col0, T.mat);
         tma_load_3d_pair(b + kBox, mapR, bar, k0, col0 + 64, T.mat);
       }
@@ -192,20 +222,30 @@ DM_DEV void producer(const GemmArgs& g, uint32_t rank, uint8_t* sA, uint8_t* sB,
   }
 }
 
-template <bool FULL>
+template <int KIND>
 DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* full_bar,
                        uint64_t* empty_bar, uint64_t* tfull, uint64_t* tempty,
                        uint64_t* drain_bar, uint32_t tmem_base, volatile int* abort_flag) {
-  constexpr uint32_t idesc = idesc_bf16(kTileM, kTileN, FULL);
+  constexpr uint32_t idesc = idesc_bf16(kTileM, kTileN, Kind<KIND>::l_mn, Kind<KIND>::r_mn);
   const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
   const int clusters = int(cluster_count_x());
   int stage = 0;
   uint32_t phase = 0;
   int it = 0;
   for (int t = int(cluster_id_x()); t < g.total_tiles; t += clusters, ++it) {
-    const TileInfo T = decode_tile<FULL>(g, g.tile_base + t);
+    const TileInfo T = decode_tile<KIND>(g, g.tile_base + t);
     const Bucket& B = g.buckets[T.bucket];
-    const int KB = (k_extent<FULL>(g, B) + kBK - 1) / kBK;
+    const int KB = (k_extent<KIND>(g, B) + kBK - 1) / kBK;
+    // Descriptors of stage 0, K-step 0; the start-address field (bits 0-13,
+    // address >> 4) then advances by a constant per stage and per K-step of
+    // 16 elements: K-major 32 bytes along the swizzled 128-byte row (8-row
+    // groups 1 KB apart); MN-major 2 KB = 16 K-rows (64-element atoms 8 KB
+    // apart, LBO; 8-row K groups 1 KB apart, SBO).  Shared-memory addresses
+    // stay below 256 KB, so the field never carries into the next one.
+    const uint64_t a_desc = sdesc_sw128(a0, Kind<KIND>::l_mn ? kBox : 16, 1024);
+    const uint64_t b_desc = sdesc_sw128(b0, Kind<KIND>::r_mn ? kBox : 16, 1024);
+    constexpr uint32_t a_kstep = Kind<KIND>::l_mn ? (2048u >> 4) : (32u >> 4);
+    constexpr uint32_t b_kstep = Kind<KIND>::r_mn ? (2048u >> 4) : (32u >> 4);
     const int acc = it & 1;
     const uint32_t aph = uint32_t(it >> 1) & 1u;
     if (!mbar_wait_cluster(&tempty[acc], aph ^ 1u, abort_flag)) {
@@ -222,19 +262,11 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
         break;
       }
       tc_fence_after();
-      const uint32_t sa = a0 + uint32_t(stage * kAStage);
-      const uint32_t sb = b0 + uint32_t(stage * kBStage);
+      const uint64_t ad = a_desc + uint64_t(stage * (kAStage >> 4));
+      const uint64_t bd = b_desc + uint64_t(stage * (kBStage >> 4));
 #pragma unroll
-      for (int k = 0; k < kBK / 16; ++k) {
-        // K-major L: 16 K-elements = 32 bytes along the swizzled 128-byte row;
-        // 8-row groups 1024 bytes apart.
-        const uint64_t ad = sdesc_sw128(sa + uint32_t(k * 32), 16, 1024);
-        // MN-major R: 64-column atoms 8 KB apart (LBO), 8-row K groups 1 KB
-        // apart (SBO); 16 K-rows = 2 KB.  K-major R as for L.
-        const uint64_t bd = FULL ? sdesc_sw128(sb + uint32_t(k * 2048), kBox, 1024)
-                                 : sdesc_sw128(sb + uint32_t(k * 32), 16, 1024);
-        umma_bf16_pair(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-      }
+      for (int k = 0; k < kBK / 16; ++k)
+        umma_bf16_pair(d, ad + k * a_kstep, bd + k * b_kstep, idesc, (kb | k) != 0 ? 1u : 0u);
       umma_commit_pair(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
       if (++stage == kStages) {
         stage = 0;
@@ -294,35 +326,27 @@ DM_DEV const void* emap_of(const GemmArgs& g, const Bucket& B, int slot) {
   return g.tmaps + size_t(B.tmap + kSlots + slot) * 128;
 }
 
-// Last product of a Newton-Schulz run: O goes straight into the packed buffer
-// in the parameter's orientation (row r of the working matrix, columns
-// c0..c0+31).
+// Last product of a Newton-Schulz run: O goes straight into the packed buffer,
+// whose segments hold the parameter's orientation, as the working layout does
+// (row r, columns c0..c0+31 of a parameter with `cols` columns).
 DM_DEV void store_final_chunk(const GemmArgs& g, const Bucket& B, const TileInfo& T, int r,
-                              int c0, const float (&o)[32]) {
-  const int m = B.m, n = B.n;
+                              int c0, int cols, const float (&o)[32]) {
   const InternalMat im = g.imat[B.first + T.mat];
-  __nv_bfloat16* P = g.packed + im.packed_off;
-  if (!im.transposed) {
-    __nv_bfloat16* row = P + (long long)r * n;
-    if ((n & 7) == 0 && c0 + 32 <= n) {
-      store_bf16x32(row + c0, o);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (c0 + j < n) row[c0 + j] = __float2bfloat16_rn(o[j]);
-    }
+  __nv_bfloat16* row = g.packed + im.packed_off + (long long)r * cols;
+  if ((cols & 7) == 0 && c0 + 32 <= cols) {
+    store_bf16x32(row + c0, o);
   } else {
-    // parameter is (n, m): element (r, c) of X goes to row c, column r
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (c0 + j < n) P[(long long)(c0 + j) * m + r] = __float2bfloat16_rn(o[j]);
+      if (c0 + j < cols) row[c0 + j] = __float2bfloat16_rn(o[j]);
   }
 }
 
-template <bool FULL>
+template <int KIND>
 DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t* tempty,
                      uint64_t* aux_bar_all, uint32_t epi_smem, uint32_t tmem_base,
                      volatile int* abort_flag) {
+  constexpr bool FULL = Kind<KIND>::full;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;          // TMEM lane quarter this warp may read
   const int h = (warp - 2) >> 2;   // which 128-column half of the tile
@@ -348,7 +372,7 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
   // lane 0: TMA load of chunk cc of tile T's a*X operand into buffer cc & 1
   auto issue_aux = [&](const TileInfo& T, const Bucket& B, int cc) {
     const int c0 = T.tj * kTileN + h * 128 + cc * 32;
-    if (c0 >= B.n) return;
+    if (c0 >= (Kind<KIND>::tall ? B.m : B.n)) return;
     const int b = cc & 1;
     mbar_arrive_expect_tx(&aux_bar[b], kEpiBufBytes);
     tma_load_3d_u32(buf(b), emap_of(g, B, g.sAux), smem_u32(&aux_bar[b]), c0,
@@ -357,7 +381,7 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
 
   int t = int(cluster_id_x());
   if (aux_tma && t < g.total_tiles && lane == 0) {
-    const TileInfo T = decode_tile<FULL>(g, g.tile_base + t);
+    const TileInfo T = decode_tile<KIND>(g, g.tile_base + t);
     const Bucket& B = g.buckets[T.bucket];
     acquire_maps(T.bucket, B);
     issue_aux(T, B, 0);
@@ -366,7 +390,7 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
   bool ok = true;
   int it = 0;
   for (; ok && t < g.total_tiles; t += clusters, ++it) {
-    const TileInfo T = decode_tile<FULL>(g, g.tile_base + t);
+    const TileInfo T = decode_tile<KIND>(g, g.tile_base + t);
     const Bucket& B = g.buckets[T.bucket];
     if (lane == 0) acquire_maps(T.bucket, B);
     const int acc = it & 1;
@@ -379,7 +403,9 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
       break;
     }
     tc_fence_after();
-    const int ncols = FULL ? B.n : B.m;
+    // output extent: m x m (symmetric), X m x n or Y n x m (full)
+    const int nrows = FULL && Kind<KIND>::tall ? B.n : B.m;
+    const int ncols = FULL && !Kind<KIND>::tall ? B.n : B.m;
     const int rg0 = T.ti * kTileM + r_loc;  // first output row of this warp's chunks
     const int r = rg0 + lane;
     const float alpha =
@@ -429,7 +455,7 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
             bulk_commit();
           }
         } else {
-          if (r < B.m) store_final_chunk(g, B, T, r, c0, o);
+          if (r < nrows) store_final_chunk(g, B, T, r, c0, ncols, o);
           __syncwarp();  // every lane is done reading buffer b
         }
         // operand of chunk cc + 2 into the buffer just used
@@ -490,7 +516,7 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
     if (lane == 0) mbar_arrive_cluster(leader_tempty + uint32_t(acc) * 8u);
     // operands of the next tile's first two chunks
     if (ok && aux_tma && lane == 0 && t + clusters < g.total_tiles) {
-      const TileInfo Tn = decode_tile<FULL>(g, g.tile_base + t + clusters);
+      const TileInfo Tn = decode_tile<KIND>(g, g.tile_base + t + clusters);
       const Bucket& Bn = g.buckets[Tn.bucket];
       acquire_maps(Tn.bucket, Bn);
       if (!g.final_out) bulk_wait_read<0>();
@@ -503,7 +529,7 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
   __syncwarp();
 }
 
-template <bool FULL>
+template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -546,13 +572,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   const uint32_t tmem_base = *tmem_slot;
 
   if (threadIdx.x == 0) {
-    producer<FULL>(g, rank, sA, sB, full_bar, empty_bar, abort_flag);
+    producer<KIND>(g, rank, sA, sB, full_bar, empty_bar, abort_flag);
   } else if (threadIdx.x == 32) {
     if (rank == 0)
-      mma_issuer<FULL>(g, sA, sB, full_bar, empty_bar, tfull, tempty, drain_bar, tmem_base,
+      mma_issuer<KIND>(g, sA, sB, full_bar, empty_bar, tfull, tempty, drain_bar, tmem_base,
                        abort_flag);
   } else if (warp >= 2) {
-    epilogue<FULL>(g, rank, tfull, tempty, aux_bar, smem_u32(sE), tmem_base, abort_flag);
+    epilogue<KIND>(g, rank, tfull, tempty, aux_bar, smem_u32(sE), tmem_base, abort_flag);
   }
 
   __syncthreads();
@@ -630,33 +656,44 @@ cudaError_t launch_diag_shift(const Bucket* buckets, int n_buckets, int first_in
 
 size_t ns_gemm_smem_bytes() { return kSmemBytes; }
 
-cudaError_t ns_gemm_prepare(int num_sms, int* max_clusters) {
-  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<false>,
+template <int KIND>
+cudaError_t prepare_kind(int num_sms, int* max_clusters) {
+  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<KIND>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(kSmemBytes));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(ns_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(kSmemBytes));
-  if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg = pair_config(num_sms / 2, nullptr, &attr);
-  int n0 = 0, n1 = 0;
-  e = cudaOccupancyMaxActiveClusters(&n0, ns_gemm_kernel<false>, &cfg);
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, ns_gemm_kernel<KIND>, &cfg);
   if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveClusters(&n1, ns_gemm_kernel<true>, &cfg);
+  if (n < *max_clusters) *max_clusters = n;
+  return cudaSuccess;
+}
+
+cudaError_t ns_gemm_prepare(int num_sms, int* max_clusters) {
+  *max_clusters = num_sms / 2;
+  cudaError_t e = prepare_kind<kSymK>(num_sms, max_clusters);
+  if (e == cudaSuccess) e = prepare_kind<kSymMN>(num_sms, max_clusters);
+  if (e == cudaSuccess) e = prepare_kind<kFullWide>(num_sms, max_clusters);
+  if (e == cudaSuccess) e = prepare_kind<kFullTall>(num_sms, max_clusters);
   if (e != cudaSuccess) return e;
-  *max_clusters = n0 < n1 ? n0 : n1;
   if (*max_clusters < 1) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
 }
 
-cudaError_t launch_ns_gemm(const GemmArgs& g, bool full, int max_clusters, cudaStream_t s) {
+cudaError_t launch_ns_gemm(const GemmArgs& g, int kind, int max_clusters, cudaStream_t s) {
   if (g.total_tiles <= 0 || g.n_buckets <= 0) return cudaSuccess;
   const int clusters = g.total_tiles < max_clusters ? g.total_tiles : max_clusters;
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg = pair_config(clusters, s, &attr);
-  if (full) return counted(cudaLaunchKernelEx(&cfg, ns_gemm_kernel<true>, g));
-  return counted(cudaLaunchKernelEx(&cfg, ns_gemm_kernel<false>, g));
+  switch (kind) {
+    case kSymK: return counted(cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kSymK>, g));
+    case kSymMN: return counted(cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kSymMN>, g));
+    case kFullWide: return counted(cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kFullWide>, g));
+    case kFullTall: return counted(cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kFullTall>, g));
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace dm

@@ -324,11 +324,13 @@ DM_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_byt
 
 // Instruction descriptor, kind::f16: fp32 D, bf16 A and B, dense.
 //   bits 4-5 D format (1 = f32)    bits 7-9 A format (1 = bf16)
-//   bits 10-12 B format (1 = bf16) bit 15 A major (0 = K)  bit 16 B major (1 = MN)
+//   bits 10-12 B format (1 = bf16) bit 15 A major (1 = MN)  bit 16 B major (1 = MN)
 //   bits 17-22 N >> 3              bits 24-28 M >> 4
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
+                                                  bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 }  // namespace dm

@@ -10,7 +10,7 @@ namespace dm {
 // matrix in chunks of kChunk elements; one block per chunk.
 constexpr int kChunk = 8192;
 constexpr int kEwThreads = 256;
-// Relayout (normalise + optional transpose into the working layout): 64x64 tiles.
+// Relayout (normalise into the working layout, a padded-pitch copy): 64x64 tiles.
 constexpr int kRelayTile = 64;
 
 // Per-bucket buffers.  Slots 0-1 hold m x n working matrices X, slots 2-7 hold
@@ -42,15 +42,18 @@ struct EwMat {
   int n_chunks;
   int tiles_r, tiles_c;    // relayout tile grid over (rows, cols)
   int pitch_x;             // row pitch of the working layout (elements)
-  int transposed;          // rows > cols: working matrix is the transpose
+  int transposed;          // rows > cols: Newton-Schulz's X is the transpose of the
+                           // parameter (the working layout keeps the parameter's own)
   int flags;
   float upd_scale;         // sqrt(max(1, rows / cols))
   int active;              // 0 for empty matrices (rows or cols == 0)
 };
 
-// Matrices with the same working shape (m, n) form a bucket; each bucket's
-// buffers hold `count` matrices back to back at a fixed stride, so one 3-D
-// tensor map per buffer covers the whole bucket.
+// Matrices with the same working shape (m, n) and orientation form a bucket;
+// each bucket's buffers hold `count` matrices back to back at a fixed stride,
+// so one 3-D tensor map per buffer covers the whole bucket.  The m x n slots
+// keep the parameter's orientation: X (m x n) for a wide or square parameter,
+// Y = X^T (n x m) for a tall one (`tall`).
 struct Bucket {
   int m, n, count, first;        // first: internal index of the bucket's first matrix
   int pitch_x, pitch_m;          // row pitch (elements) of X slots / m x m slots
@@ -61,7 +64,7 @@ struct Bucket {
   int full_ti, full_tj;          // tile grid of an m x n product
   int sym_begin;                 // first tile of this bucket in a symmetric launch
   int full_begin;                // first tile of this bucket in a full launch
-  int pad_;
+  int tall;                      // rows > cols: X slots hold Y = X^T (n rows x m columns)
 };
 
 // One tensor of an AdamW group (any shape, contiguous), walked in chunks.
@@ -92,6 +95,14 @@ struct InternalMat {
   int transposed;
 };
 
+// Kinds of product launch; one launch covers buckets of one orientation, so
+// the operand layouts and the instruction descriptor are compile-time.
+//   kSymK     symmetric L R^T, both operands K-major (wide/square X X^T, m x m products)
+//   kSymMN    symmetric Y^T Y of tall buckets, both operands MN-major
+//   kFullWide X' = alpha X + gamma L X  (L m x m K-major, X MN-major)
+//   kFullTall Y' = alpha Y + gamma Y L  (Y K-major, L symmetric, K-major)
+enum ProductKind : int { kSymK = 0, kSymMN = 1, kFullWide = 2, kFullTall = 3 };
+
 // Tile shape of the Newton-Schulz products: a CTA pair computes a 256 x 256
 // tile; each CTA holds 128 of its rows (and loads half of its columns' operand).
 constexpr int kTileM = 256, kTileN = 256, kCtaM = 128, kBK = 64;
@@ -101,6 +112,9 @@ constexpr int kTileM = 256, kTileN = 256, kCtaM = 128, kBK = 64;
 //     out = alpha * I + beta * aux + gamma * (L R^T)
 //   full product (m x n output):
 //     out = alpha * aux + gamma * (L R)        (L: m x m, R: m x n)
+//     for a tall bucket the X slots hold Y = X^T, and the same launch computes
+//     Y' = alpha * Y + gamma * (Y L) instead (L symmetric): sL names the m x m
+//     operand and sR the X slot in both cases
 // When `shift` is set, alpha becomes alpha + shift_sign * shift[matrix] per
 // matrix (internal order).
 struct GemmArgs {
