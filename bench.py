@@ -379,24 +379,27 @@ def run_gpu(args, rank, world, local_rank):
         h2d_stream = torch.cuda.Stream(device=dev)
         d2h_stream = torch.cuda.Stream(device=dev)
 
-        def e2e_steps(nsteps):
+        def e2e_steps(nsteps, spans=None):
+            # spans: per step (h2d start, h2d end, step start, step end, d2h start, d2h end)
             step_done = [None, None]   # last step that read gradient buffer b
             d2h_done = [None, None]    # last copy out of snapshot buffer b
             last = None
+            ev = lambda: torch.cuda.Event(enable_timing=spans is not None)
             for k in range(nsteps):
                 b = k % 2
+                sp = [ev() for _ in range(6)]
                 with torch.cuda.stream(h2d_stream):
                     if step_done[b] is not None:
                         h2d_stream.wait_event(step_done[b])
+                    sp[0].record(h2d_stream)
                     G_dev[b].flat.copy_(G_host.flat, non_blocking=True)
-                    g_ready = torch.cuda.Event()
-                    g_ready.record(h2d_stream)
-                stream.wait_event(g_ready)
+                    sp[1].record(h2d_stream)
+                stream.wait_event(sp[1])
+                sp[2].record(stream)
                 owner.step(G_dev[b].views, M.views, W.views, lr=0.02, beta=0.95,
                            ns_steps=args.ns_steps, stream=stream)
-                done = torch.cuda.Event()
-                done.record(stream)
-                step_done[b] = done
+                sp[3].record(stream)
+                step_done[b] = sp[3]
                 with torch.cuda.stream(stream):
                     if d2h_done[b] is not None:
                         stream.wait_event(d2h_done[b])
@@ -405,11 +408,13 @@ def run_gpu(args, rank, world, local_rank):
                     snap.record(stream)
                 with torch.cuda.stream(d2h_stream):
                     d2h_stream.wait_event(snap)
+                    sp[4].record(d2h_stream)
                     W_host.flat.copy_(W_snap[b].flat, non_blocking=True)
-                    out = torch.cuda.Event()
-                    out.record(d2h_stream)
-                    d2h_done[b] = out
-                last = out
+                    sp[5].record(d2h_stream)
+                    d2h_done[b] = sp[5]
+                last = sp[5]
+                if spans is not None:
+                    spans.append(sp)
             return last
 
         e2e_steps(max(2, min(args.warmup, 3)))
@@ -418,7 +423,8 @@ def run_gpu(args, rank, world, local_rank):
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(h2d_stream)
         stream.wait_event(e0)
-        last = e2e_steps(args.steps)
+        spans = []
+        last = e2e_steps(args.steps, spans)
         stream.wait_event(last)
         e1.record(stream)
         barrier()
@@ -426,8 +432,15 @@ def run_gpu(args, rank, world, local_rank):
         if st != dmuon.OK:
             raise RuntimeError(f"e2e steps failed: {dmuon.status_string(st)}")
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
+        mean = lambda i, j: sum(sp[i].elapsed_time(sp[j]) for sp in spans) / len(spans)
+        h2d_ms, step_ms_e2e, d2h_ms = mean(0, 1), mean(2, 3), mean(4, 5)
         e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h)}
+               "d2h_bytes_per_step": int(d2h),
+               "note": "copies of step k+1's gradients in and step k-1's weights out overlap "
+                       "step k; the first copy in and the last copy out are not hidden",
+               "h2d_ms": h2d_ms, "h2d_gbs": h2d / (h2d_ms * 1e-3) / 1e9,
+               "d2h_ms": d2h_ms, "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9,
+               "step_ms": step_ms_e2e}
         del G_host, W_host, G_dev, W_snap
 
 

@@ -159,10 +159,11 @@ int dmuon_unpack_update(int n, const dmuon_shape* shp, void* const* weight,
  * dmuon_ns_batched(use_pack_norms = 1) with the default coefficients and
  * eps = 1e-7, then dmuon_unpack_update, enqueued on `stream`.
  * With the standard variant, ns_steps >= 1 and two or more distinct working
- * shapes, the step overlaps its memory-bound kernels with the tensor-core
- * products: the shape with the most elements is packed and relaid out while
- * the other matrices are orthogonalised, and the other matrices' weights are
- * updated while it is orthogonalised.  That work runs on a lowest-priority
+ * shapes (or orientations), the step overlaps its memory-bound kernels with
+ * the tensor-core products: it visits the shape groups smallest first, and
+ * while one group is orthogonalised the later groups are packed and relaid
+ * out and the earlier groups' weights are updated, so that only the first
+ * group's pack and the last group's update run alone.  That work runs on a lowest-priority
  * stream the library creates once per device, ordered against `stream` with
  * events; when the call returns, all of it is ordered before any later work
  * on `stream`.  Results are identical to the three separate calls.

@@ -92,12 +92,9 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
   P.tiles_c.assign(n, 0);
 
   // buckets keyed by (gram, m, n, tall); standard first, each group in
-  // first-seen order, except that the standard bucket with the most elements
-  // goes last (a whole step overlaps its memory-bound work with the others'
-  // products)
+  // first-seen order
   using Key = std::tuple<int, int, int, int>;
   std::map<Key, int> key_to_b;
-  std::map<Key, long long> key_elems;
   std::vector<Key> order;
   for (int i = 0; i < n; ++i) {
     if (!shape_ok(shp[i])) return DMUON_ERR_INVALID_ARG;
@@ -112,7 +109,6 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
       key_to_b[key] = -1;
       order.push_back(key);
     }
-    key_elems[key] += r * c;
   }
   // within each group, wide/square buckets before tall ones, so that every
   // product launch splits into few runs of one orientation
@@ -120,15 +116,6 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
     return std::make_pair(std::get<0>(a), std::get<3>(a)) <
            std::make_pair(std::get<0>(b), std::get<3>(b));
   });
-  {
-    int n_std = 0, big = -1;
-    for (size_t b = 0; b < order.size(); ++b) {
-      if (std::get<0>(order[b]) != 0) break;
-      ++n_std;
-      if (big < 0 || key_elems[order[b]] > key_elems[order[size_t(big)]]) big = int(b);
-    }
-    if (big >= 0) std::rotate(order.begin() + big, order.begin() + big + 1, order.begin() + n_std);
-  }
   for (size_t b = 0; b < order.size(); ++b) {
     key_to_b[order[b]] = int(b);
     BucketPlan bp;
@@ -601,15 +588,18 @@ bool ns_gram(const GemmLauncher& L, const Request& R) {
 // Events used to order the two streams of an overlapped step; released when
 // the call returns (the driver keeps a pending event alive until it fires).
 struct EventSet {
-  cudaEvent_t e[4] = {};
-  int made = 0;
-  bool create() {
-    for (; made < 4; ++made)
-      if (cudaEventCreateWithFlags(&e[made], cudaEventDisableTiming) != cudaSuccess) return false;
+  std::vector<cudaEvent_t> e;
+  bool create(int count) {
+    e.reserve(size_t(count));
+    for (int i = 0; i < count; ++i) {
+      cudaEvent_t x = nullptr;
+      if (cudaEventCreateWithFlags(&x, cudaEventDisableTiming) != cudaSuccess) return false;
+      e.push_back(x);
+    }
     return true;
   }
   ~EventSet() {
-    for (int i = 0; i < made; ++i) cudaEventDestroy(e[i]);
+    for (cudaEvent_t x : e) cudaEventDestroy(x);
   }
 };
 
@@ -650,40 +640,51 @@ int run(const Request& R) {
     return r;
   };
 
-  // A whole standard step over two or more buckets overlaps its memory-bound
-  // kernels with the products on a second, low-priority stream: the largest
-  // bucket (last) is packed and relaid out while the other buckets' products
-  // run, and the other buckets' weights are updated while its products run.
-  //   stream s : pack, norm, relayout of G1 | products G1 |   wait   | products G2, update G2 | join
-  //   aux      :                            | pack, norm, relayout G2 | update G1
+  // A whole standard step over two or more buckets runs as a pipeline over the
+  // buckets, smallest first, with the memory-bound kernels on a second,
+  // low-priority stream: while one bucket's products run, the later buckets
+  // are packed and relaid out and the earlier buckets' weights are updated.
+  // Only the first bucket's pack and the last bucket's update are exposed.
+  //   stream s : mb(0) | NS(0) | NS(1) | ... | NS(G-1), update(G-1) | join
+  //   aux      :       | mb(1), mb(2), ..., mb(G-1), update(0), ..., update(G-2)
+  // (mb = momentum + pack, norm finish, relayout; NS(k) waits for mb(k),
+  // update(k) for NS(k))
   const bool overlap = R.do_pack && R.do_ns && R.do_update && R.ns_steps > 0 && P.n_std >= 2 &&
                        P.n_std == nb && D.aux != nullptr;
   if (overlap) {
-    EventSet ev;
-    if (!ev.create()) return DMUON_ERR_CUDA;
-    const int split = P.n_std - 1;
-    const EwRange g1 = range_of(0, split), g2 = range_of(split, nb);
+    std::vector<int> ord(static_cast<size_t>(nb));
+    for (int b = 0; b < nb; ++b) ord[size_t(b)] = b;
+    std::stable_sort(ord.begin(), ord.end(), [&](int a, int b) {
+      return P.buckets[a].chunks < P.buckets[b].chunks;
+    });
+    EventSet ev;  // [0, nb): mb(k) done; [nb, 2nb): NS(k) done; 2nb: aux done
+    if (!ev.create(2 * nb + 1)) return DMUON_ERR_CUDA;
     cudaStream_t x = D.aux;
-    if (launch_momentum_pack(g1, gbf16, R.beta, packed, partials, s) != cudaSuccess ||
-        launch_norm_finalize(g1, partials, R.eps, inv, s) != cudaSuccess ||
-        launch_relayout(g1, packed, inv, s) != cudaSuccess || cudaEventRecord(ev.e[0], s) != cudaSuccess)
-      return DMUON_ERR_CUDA;
-    if (cudaStreamWaitEvent(x, ev.e[0], 0) != cudaSuccess ||
-        launch_momentum_pack(g2, gbf16, R.beta, packed, partials, x) != cudaSuccess ||
-        launch_norm_finalize(g2, partials, R.eps, inv, x) != cudaSuccess ||
-        launch_relayout(g2, packed, inv, x) != cudaSuccess || cudaEventRecord(ev.e[1], x) != cudaSuccess)
-      return DMUON_ERR_CUDA;
-    if (!ns_standard(GemmLauncher(P, R, D.max_clusters, ws, 0, split, s), R, P, ws) ||
-        cudaEventRecord(ev.e[2], s) != cudaSuccess)
-      return DMUON_ERR_CUDA;
-    if (cudaStreamWaitEvent(x, ev.e[2], 0) != cudaSuccess ||
-        launch_update(g1, wbf16, R.lr, packed, x) != cudaSuccess ||
-        cudaEventRecord(ev.e[3], x) != cudaSuccess)
-      return DMUON_ERR_CUDA;
-    if (cudaStreamWaitEvent(s, ev.e[1], 0) != cudaSuccess ||
-        !ns_standard(GemmLauncher(P, R, D.max_clusters, ws, split, nb, s), R, P, ws) ||
-        launch_update(g2, wbf16, R.lr, packed, s) != cudaSuccess ||
-        cudaStreamWaitEvent(s, ev.e[3], 0) != cudaSuccess)
+    auto mb = [&](int k, cudaStream_t st) {
+      const EwRange r = range_of(ord[k], ord[k] + 1);
+      return launch_momentum_pack(r, gbf16, R.beta, packed, partials, st) == cudaSuccess &&
+             launch_norm_finalize(r, partials, R.eps, inv, st) == cudaSuccess &&
+             launch_relayout(r, packed, inv, st) == cudaSuccess &&
+             cudaEventRecord(ev.e[k], st) == cudaSuccess;
+    };
+    if (!mb(0, s)) return DMUON_ERR_CUDA;
+    if (cudaStreamWaitEvent(x, ev.e[0], 0) != cudaSuccess) return DMUON_ERR_CUDA;
+    for (int k = 1; k < nb; ++k)
+      if (!mb(k, x)) return DMUON_ERR_CUDA;
+    for (int k = 0; k < nb; ++k) {
+      if (k > 0 && cudaStreamWaitEvent(s, ev.e[k], 0) != cudaSuccess) return DMUON_ERR_CUDA;
+      if (!ns_standard(GemmLauncher(P, R, D.max_clusters, ws, ord[k], ord[k] + 1, s), R, P, ws) ||
+          cudaEventRecord(ev.e[nb + k], s) != cudaSuccess)
+        return DMUON_ERR_CUDA;
+    }
+    for (int k = 0; k + 1 < nb; ++k)
+      if (cudaStreamWaitEvent(x, ev.e[nb + k], 0) != cudaSuccess ||
+          launch_update(range_of(ord[k], ord[k] + 1), wbf16, R.lr, packed, x) != cudaSuccess)
+        return DMUON_ERR_CUDA;
+    if (cudaEventRecord(ev.e[2 * nb], x) != cudaSuccess ||
+        launch_update(range_of(ord[nb - 1], ord[nb - 1] + 1), wbf16, R.lr, packed, s) !=
+            cudaSuccess ||
+        cudaStreamWaitEvent(s, ev.e[2 * nb], 0) != cudaSuccess)
       return DMUON_ERR_CUDA;
     return DMUON_OK;
   }
