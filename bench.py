@@ -447,10 +447,19 @@ def run_gpu(args, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     tr = traffic_record()
+    if tr is not None and (tr.get("workload") != args.workload or tr.get("ns_steps") != args.ns_steps
+                           or args.variant != 0):
+        tr = None   # the ncu figure covers one workload and configuration only
+    # one roofline unit = one Newton-Schulz phase: all product launches of one step
     roofline = {"bound": "tensor", "kernel": "ns_gemm_kernel (all Newton-Schulz products)",
+                "unit_of_work": "one Newton-Schulz phase (all product launches of one step)",
                 "achieved": achieved_tflops, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved_tflops / peak, "peak_source": f"{peak_src} bf16 sustained",
-                "traffic": None if tr is None else tr.get("dram_bytes_per_launch"),
+                "traffic": None if tr is None else tr.get("dram_bytes_per_ns_phase"),
+                # per matrix and iteration: X read twice and X' written (6mn bytes),
+                # A and B each written once and read once (8m^2 bytes), bf16
+                "algorithmic_bytes": None if args.variant != 0 else float(args.ns_steps * sum(
+                    6 * min(r, c) * max(r, c) + 8 * min(r, c) ** 2 for r, c in shapes)),
                 "flops_per_step": ns_flops}
     elem_bytes = {"pack": (2 if w.grad_dtype == torch.bfloat16 else 4) + 4 + 4 + 2,
                   "update": 2 + 2 * (2 if w.weight_dtype == torch.bfloat16 else 4)}
