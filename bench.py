@@ -329,6 +329,43 @@ def run_gpu(args, rank, world, local_rank):
     ns_mean = sum(ns_ms) / len(ns_ms)
     achieved_tflops = ns_flops / (ns_mean * 1e-3) / 1e12
 
+    # ---- owners (workloads with an LPT owner partition): each owner's
+    # Newton-Schulz as its own call on its segments of the packed buffer, back
+    # to back, against the grouped call above -- the single-GPU picture of the
+    # pages' balanced ownership (the slowest owner bounds a distributed step).
+    owners = None
+    if w.n_owners > 1:
+        groups = [[i for i in range(n) if owner.owner_of[i] == k] for k in range(w.n_owners)]
+        groups = [gk for gk in groups if gk]
+        ws_max = max(dmuon.workspace_bytes([shapes[i] for i in gk], args.variant) for gk in groups)
+        ws_o = torch.zeros(ws_max, dtype=torch.uint8, device=dev)
+
+        def owner_ns(gk):
+            dmuon.ns_batched([shapes[i] for i in gk], owner.packed, [owner.offsets[i] for i in gk],
+                             ws_o, ns_steps=args.ns_steps, variant=args.variant, stream=stream)
+
+        for gk in groups:
+            owner_ns(gk)
+        barrier()
+        oev = [torch.cuda.Event(enable_timing=True) for _ in range(len(groups) + 1)]
+        with torch.cuda.stream(stream):
+            oev[0].record(stream)
+            for k, gk in enumerate(groups):
+                owner_ns(gk)
+                oev[k + 1].record(stream)
+        barrier()
+        st = dmuon.stream_status(ws_o, stream)
+        if st != dmuon.OK:
+            raise RuntimeError(f"per-owner NS failed: {dmuon.status_string(st)}")
+        o_ms = [oev[k].elapsed_time(oev[k + 1]) for k in range(len(groups))]
+        o_elems = [sum(shapes[i][0] * shapes[i][1] for i in gk) for gk in groups]
+        owners = {"n_owners": len(groups), "ns_ms": o_ms, "elements": o_elems,
+                  "back_to_back_ms": sum(o_ms), "grouped_ns_ms": ns_mean,
+                  "max_over_mean": max(o_ms) / (sum(o_ms) / len(o_ms)),
+                  "note": "each owner's Newton-Schulz alone (norms from the packed values), "
+                          "back to back, vs all owners in one grouped call"}
+        del ws_o
+
     # ---- AdamW for the parameters outside the Muon set (embedding, head, norms),
     # timed on its own: bf16 parameters and gradients, fp32 moments.
     adamw = None
@@ -498,6 +535,7 @@ def run_gpu(args, rank, world, local_rank):
         "e2e": e2e,
         "gpu_launches": timed_launches,
         "adamw": adamw,
+        "owners": owners,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
