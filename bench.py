@@ -245,6 +245,7 @@ def run_gpu(args, rank, world, local_rank):
     shapes = w.shapes()
     n = len(shapes)
     owner = dmuon.MuonOwner(shapes, n_owners=w.n_owners, variant=args.variant, device=dev)
+    packed_elems = owner.packed.numel()
     G = wl.alloc_flat(shapes, w.grad_dtype, dev)
     M = wl.alloc_flat(shapes, torch.float32, dev)
     W = wl.alloc_flat(shapes, w.weight_dtype, dev)
@@ -400,10 +401,13 @@ def run_gpu(args, rank, world, local_rank):
 
     # ---- end to end through dmuon_muon_step with host buffers.  Every step copies
     # its gradients in from pinned host memory and its updated weights back out.
-    # The copies are pipelined with the compute the way a training loop would:
-    # the next step's gradients land in a second device buffer while the current
-    # step runs, and the updated weights are snapshotted on the device and copied
-    # out while the next step runs.  All copies sit inside the timed region.
+    # The copies are pipelined with the compute the way a training loop would,
+    # per group of consecutive layers (one owner and one dmuon_muon_step call
+    # per group): a group's gradients are copied in while the previous group
+    # computes, its updated weights are snapshotted on the device and copied
+    # out while the next group computes, and the next step's copies in use a
+    # second device buffer.  Only the first group's copy in and the last
+    # group's copy out are not hidden.  All copies sit inside the timed region.
     e2e = None
     if not args.no_e2e:
         G_host = wl.alloc_flat(shapes, w.grad_dtype, "cpu", pin=True, zero=False)
@@ -415,41 +419,64 @@ def run_gpu(args, rank, world, local_rank):
         W_snap = [wl.alloc_flat(shapes, w.weight_dtype, dev, zero=False) for _ in range(2)]
         h2d_stream = torch.cuda.Stream(device=dev)
         d2h_stream = torch.cuda.Stream(device=dev)
+        # groups of whole layers, each a contiguous range of every flat buffer
+        per_layer = max(1, n // max(1, w.layers))
+        n_groups = max(1, min(args.e2e_groups, n // per_layer))
+        bounds = [round(g_ * (n // per_layer) / n_groups) * per_layer for g_ in range(n_groups)] + [n]
+        gsets = [(bounds[j], bounds[j + 1]) for j in range(n_groups) if bounds[j] < bounds[j + 1]]
+        del owner   # the groups' owners take its place
+        torch.cuda.empty_cache()
+        g_owner = [dmuon.MuonOwner(shapes[i0:i1], n_owners=w.n_owners, variant=args.variant,
+                                   device=dev) for i0, i1 in gsets]
+
+        def span(fs, i0, i1):
+            o1 = fs.offsets[i1] if i1 < n else fs.flat.numel()
+            return fs.flat[fs.offsets[i0]:o1]
 
         def e2e_steps(nsteps, spans=None):
             # spans: per step (h2d start, h2d end, step start, step end, d2h start, d2h end)
-            step_done = [None, None]   # last step that read gradient buffer b
-            d2h_done = [None, None]    # last copy out of snapshot buffer b
+            done = [[None] * len(gsets) for _ in range(2)]   # last step that read G_dev[b], group j
+            out = [[None] * len(gsets) for _ in range(2)]    # last copy out of W_snap[b], group j
             last = None
             ev = lambda: torch.cuda.Event(enable_timing=spans is not None)
             for k in range(nsteps):
                 b = k % 2
                 sp = [ev() for _ in range(6)]
-                with torch.cuda.stream(h2d_stream):
-                    if step_done[b] is not None:
-                        h2d_stream.wait_event(step_done[b])
-                    sp[0].record(h2d_stream)
-                    G_dev[b].flat.copy_(G_host.flat, non_blocking=True)
-                    sp[1].record(h2d_stream)
-                stream.wait_event(sp[1])
-                sp[2].record(stream)
-                owner.step(G_dev[b].views, M.views, W.views, lr=0.02, beta=0.95,
-                           ns_steps=args.ns_steps, stream=stream)
-                sp[3].record(stream)
-                step_done[b] = sp[3]
-                with torch.cuda.stream(stream):
-                    if d2h_done[b] is not None:
-                        stream.wait_event(d2h_done[b])
-                    W_snap[b].flat.copy_(W.flat, non_blocking=True)
-                    snap = torch.cuda.Event()
-                    snap.record(stream)
-                with torch.cuda.stream(d2h_stream):
-                    d2h_stream.wait_event(snap)
-                    sp[4].record(d2h_stream)
-                    W_host.flat.copy_(W_snap[b].flat, non_blocking=True)
-                    sp[5].record(d2h_stream)
-                    d2h_done[b] = sp[5]
-                last = sp[5]
+                for j, (i0, i1) in enumerate(gsets):
+                    with torch.cuda.stream(h2d_stream):
+                        if done[b][j] is not None:
+                            h2d_stream.wait_event(done[b][j])
+                        if j == 0:
+                            sp[0].record(h2d_stream)
+                        span(G_dev[b], i0, i1).copy_(span(G_host, i0, i1), non_blocking=True)
+                        g_in = ev()
+                        g_in.record(h2d_stream)
+                    stream.wait_event(g_in)
+                    if j == 0:
+                        sp[2].record(stream)
+                    g_owner[j].step(G_dev[b].views[i0:i1], M.views[i0:i1], W.views[i0:i1],
+                                    lr=0.02, beta=0.95, ns_steps=args.ns_steps, stream=stream)
+                    d = ev()
+                    d.record(stream)
+                    done[b][j] = d
+                    with torch.cuda.stream(stream):
+                        if out[b][j] is not None:
+                            stream.wait_event(out[b][j])
+                        span(W_snap[b], i0, i1).copy_(span(W, i0, i1), non_blocking=True)
+                        snap = torch.cuda.Event()
+                        snap.record(stream)
+                    with torch.cuda.stream(d2h_stream):
+                        d2h_stream.wait_event(snap)
+                        if j == 0:
+                            sp[4].record(d2h_stream)
+                        span(W_host, i0, i1).copy_(span(W_snap[b], i0, i1), non_blocking=True)
+                        o = ev()
+                        o.record(d2h_stream)
+                        out[b][j] = o
+                    last = o
+                sp[1] = g_in
+                sp[3] = d
+                sp[5] = last
                 if spans is not None:
                     spans.append(sp)
             return last
@@ -465,20 +492,24 @@ def run_gpu(args, rank, world, local_rank):
         stream.wait_event(last)
         e1.record(stream)
         barrier()
-        st = dmuon.stream_status(owner.workspace, stream)
-        if st != dmuon.OK:
-            raise RuntimeError(f"e2e steps failed: {dmuon.status_string(st)}")
+        for go in g_owner:
+            st = dmuon.stream_status(go.workspace, stream)
+            if st != dmuon.OK:
+                raise RuntimeError(f"e2e steps failed: {dmuon.status_string(st)}")
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
         mean = lambda i, j: sum(sp[i].elapsed_time(sp[j]) for sp in spans) / len(spans)
         h2d_ms, step_ms_e2e, d2h_ms = mean(0, 1), mean(2, 3), mean(4, 5)
         e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h),
-               "note": "copies of step k+1's gradients in and step k-1's weights out overlap "
-                       "step k; the first copy in and the last copy out are not hidden",
+               "groups": len(gsets),
+               "note": f"{len(gsets)} groups of consecutive layers, one dmuon_muon_step call "
+                       "each; a group's copies in and out overlap the other groups' compute; "
+                       "only the first group's copy in and the last group's copy out are not "
+                       "hidden; h2d/d2h/step times span the groups of one step",
                "h2d_ms": h2d_ms, "h2d_gbs": h2d / (h2d_ms * 1e-3) / 1e9,
                "d2h_ms": d2h_ms, "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9,
                "step_ms": step_ms_e2e}
-        del G_host, W_host, G_dev, W_snap
+        del G_host, W_host, G_dev, W_snap, g_owner
 
 
     peaks, peak_src = load_peaks()
@@ -514,7 +545,7 @@ def run_gpu(args, rank, world, local_rank):
         "hbm_peak_gbs": hbm_peak,
     }
     resident = (G.flat.numel() * G.flat.element_size() + M.flat.numel() * 4 +
-                W.flat.numel() * W.flat.element_size() + owner.packed.numel() * 2)
+                W.flat.numel() * W.flat.element_size() + packed_elems * 2)
     line = {
         "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
@@ -559,6 +590,8 @@ def main():
     ap.add_argument("--variant", type=int, default=0, help="0 standard, 1 Gram")
     ap.add_argument("--impl", default="dmuon", choices=["dmuon", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-groups", type=int, default=4,
+                    help="layer groups of the end-to-end loop (one dmuon_muon_step call each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-launch-count", action="store_true",
                     help="accepted for older command lines; the launch count now comes "
