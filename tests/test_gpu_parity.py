@@ -20,9 +20,11 @@ pytestmark = pytest.mark.gpu
 
 NS_TOL = {0: 5e-3, 1: 2e-2, 2: 2e-2, 3: 2e-2, 5: 2e-2, 8: 4e-2}
 
+# wide and tall (rows > cols: the working layout keeps the parameter's own
+# orientation) shapes with ragged tiles in every dimension
 ODD_SHAPES = [(1, 1), (1, 5), (5, 1), (7, 300), (300, 7), (129, 257), (257, 129), (64, 64),
-              (256, 1024), (1024, 256), (1000, 1000), (96, 4096), (130, 130), (8, 8200),
-              (333, 1500)]
+              (256, 1024), (1024, 256), (1000, 1000), (96, 4096), (4096, 96), (130, 130),
+              (8, 8200), (8200, 8), (333, 1500), (1500, 333)]
 
 
 @pytest.fixture(scope="module")
@@ -193,7 +195,8 @@ def test_ns_zero_matrix_gives_zero(dm):
 
 @pytest.mark.parametrize("steps", [1, 3, 5])
 def test_gram_variant(dm, wl, steps):
-    shapes = [(128, 512), (512, 128), (200, 900), (64, 4096), (300, 300), (7, 300)]
+    shapes = [(128, 512), (512, 128), (200, 900), (900, 200), (64, 4096), (300, 300), (7, 300),
+              (300, 7)]
     ps = PackedSet(dm, shapes, variant=dm.NS_GRAM)
     ins = []
     for i, s in enumerate(shapes):
@@ -293,6 +296,15 @@ def test_muon_step_single_256x1024_fp32(dm, wl):
 def test_muon_step_mixed_projection_set(dm, wl):
     shapes = [(256, 256), (64, 256), (64, 256), (256, 256), (700, 256), (700, 256), (256, 700)]
     _muon_case(dm, wl, shapes, torch.bfloat16, torch.float32)
+
+
+def test_muon_step_several_wide_and_tall_buckets(dm, wl):
+    """Several wide and several tall buckets with ragged sizes: each product
+    runs as one launch per run of same-orientation buckets, and the whole step
+    pipelines over all buckets on two streams."""
+    shapes = [(256, 700), (700, 256), (300, 900), (900, 300), (256, 256), (129, 520),
+              (520, 129), (700, 256), (64, 1000), (1000, 64)]
+    _muon_case(dm, wl, shapes, torch.bfloat16, torch.float32, seed=17)
 
 
 def test_muon_step_gram_variant(dm, wl):
