@@ -106,6 +106,16 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def blas_name() -> str:
+    """The BLAS library numpy (and so the oracle) runs on."""
+    try:
+        import numpy as np
+        b = np.show_config(mode="dicts").get("Build Dependencies", {}).get("blas", {})
+        return f"{b.get('name', '?')} {b.get('version', '')}".strip()
+    except Exception:
+        return "unknown"
+
+
 def traffic_record():
     """DRAM bytes per launch of the product kernel from the committed ncu summary,
     valid only while the kernel source is unchanged (else None)."""
@@ -196,7 +206,7 @@ def run_reference(args, rank, world):
         "data": "synthetic", "config": {"workload": args.workload, "ns_steps": 5,
                                         "variant": "standard"},
         "cpu_baseline": {"value": v, "unit": "ms", "cores": cores, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "blas": blas_name()},
         "e2e": {"value": v, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -549,6 +559,8 @@ def run_gpu(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+        "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
+        "step_ms_max": max(step_ms),
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded normal gradients/weights shaped like the model's projections)",
         "config": {"workload": args.workload, "matrices": n, "elements": elems,
@@ -572,7 +584,7 @@ def run_gpu(args, rank, world, local_rank):
     if rank == 0 and not args.no_cpu_baseline:
         cms, desc, _ = oracle_sample(args.workload)
         line["cpu_baseline"] = {"value": cms, "unit": "ms", "cores": os.cpu_count(),
-                                "kind": "oracle", "sample": desc}
+                                "kind": "oracle", "sample": desc, "blas": blas_name()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
