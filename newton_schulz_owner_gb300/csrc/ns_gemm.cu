@@ -7,13 +7,15 @@
 //               A A        -> L = R = A, aux = A (B = b*A + c*A*A)
 //   full:       out = alpha*aux + gamma * L R              (m x n)
 //               B X        -> L = B, R = X, aux = X  (X' = a*X + B*X)
-// The standard Muon iteration is these three launches per step; the Gram
-// variant chains symmetric launches on m x m matrices.
+// The standard Muon iteration is these three products per step; the Gram
+// variant chains symmetric products on m x m matrices.
 //
 // A tall parameter (rows > cols) keeps its own layout, Y = X^T (n x m), so no
 // matrix is ever transposed in memory: X X^T = Y^T Y reads both operands
 // MN-major from Y, and X' = a*X + B*X becomes Y' = a*Y + Y*B (B symmetric)
-// with both operands K-major.
+// with both operands K-major.  The operand layouts are a template parameter
+// (ProductKind), so a product runs as one launch per run of buckets of one
+// orientation, with compile-time instruction and shared-memory descriptors.
 //
 // Work unit: a 256 x 256 output tile computed by a cluster of two CTAs on two
 // SMs with one tcgen05.mma.cta_group::2 (M=256, N=256, K=16).  Each CTA loads
