@@ -167,6 +167,11 @@ int dmuon_unpack_update(int n, const dmuon_shape* shp, void* const* weight,
  * stream the library creates once per device, ordered against `stream` with
  * events; when the call returns, all of it is ordered before any later work
  * on `stream`.  Results are identical to the three separate calls.
+ * The call can be captured into a CUDA graph (stream capture on `stream`) and
+ * replayed: its tables are written by a kernel, and the second stream joins
+ * the capture through the events.  Make one call on the device before the
+ * first capture (it sets the library up for the device); the graph then reads
+ * the buffers that were passed at capture time.
  */
 int dmuon_muon_step(int n, const dmuon_shape* shp, const void* const* grad, int grad_dt,
                     float* const* momentum, void* const* weight, int weight_dt,
