@@ -392,7 +392,6 @@ int upload_tables(const Request& R, const Plan& P) {
     E.tiles_r = P.tiles_r[i];
     E.tiles_c = P.tiles_c[i];
     E.packed_off = E.active ? R.offset[i] : 0;
-    E.transposed = r > c ? 1 : 0;
     E.upd_scale = float(std::sqrt(std::max(1.0, double(r) / double(std::max<long long>(c, 1)))));
     if (R.do_pack && E.active) {
       E.g = R.grad[i];
@@ -413,7 +412,6 @@ int upload_tables(const Request& R, const Plan& P) {
       InternalMat& M = im[P.internal_of[i]];
       M.packed_off = R.offset[i];
       M.caller = i;
-      M.transposed = E.transposed;
     }
   }
   int sym_off = 0, internal = 0;

@@ -41,9 +41,8 @@ struct EwMat {
   int rows, cols;
   int n_chunks;
   int tiles_r, tiles_c;    // relayout tile grid over (rows, cols)
-  int pitch_x;             // row pitch of the working layout (elements)
-  int transposed;          // rows > cols: Newton-Schulz's X is the transpose of the
-                           // parameter (the working layout keeps the parameter's own)
+  int pitch_x;             // row pitch of the working layout (elements); the layout
+                           // keeps the parameter's orientation (Y = X^T when rows > cols)
   int flags;
   float upd_scale;         // sqrt(max(1, rows / cols))
   int active;              // 0 for empty matrices (rows or cols == 0)
@@ -92,7 +91,7 @@ struct AdamScalars {
 struct InternalMat {
   long long packed_off;
   int caller;
-  int transposed;
+  int pad_;
 };
 
 // Kinds of product launch; one launch covers buckets of one orientation, so
