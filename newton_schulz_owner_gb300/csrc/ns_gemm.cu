@@ -141,35 +141,6 @@ DM_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&t);
 }
 
-DM_DEV void load_bf16x32(const __nv_bfloat16* p, float (&f)[32]) {
-  const uint4* q = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const uint4 u = q[v];
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
-      const float2 f2 = __bfloat1622float2(b2);
-      f[v * 8 + 2 * k] = f2.x;
-      f[v * 8 + 2 * k + 1] = f2.y;
-    }
-  }
-}
-
-DM_DEV void store_bf16x32(__nv_bfloat16* p, const float (&f)[32]) {
-  uint4* q = reinterpret_cast<uint4*>(p);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    uint4 u;
-    u.x = pack_bf16x2(f[v * 8 + 0], f[v * 8 + 1]);
-    u.y = pack_bf16x2(f[v * 8 + 2], f[v * 8 + 3]);
-    u.z = pack_bf16x2(f[v * 8 + 4], f[v * 8 + 5]);
-    u.w = pack_bf16x2(f[v * 8 + 6], f[v * 8 + 7]);
-    q[v] = u;
-  }
-}
-
 // ------------------------------------------------------------------ roles
 template <int KIND>
 DM_DEV void producer(const GemmArgs& g, uint32_t rank, uint8_t* sA, uint8_t* sB,
@@ -329,18 +300,33 @@ DM_DEV const void* emap_of(const GemmArgs& g, const Bucket& B, int slot) {
 }
 
 // Last product of a Newton-Schulz run: O goes straight into the packed buffer,
-// whose segments hold the parameter's orientation, as the working layout does
-// (row r, columns c0..c0+31 of a parameter with `cols` columns).
-DM_DEV void store_final_chunk(const GemmArgs& g, const Bucket& B, const TileInfo& T, int r,
-                              int c0, int cols, const float (&o)[32]) {
+// whose segments hold the parameter's orientation, as the working layout does.
+// The warp's 32 x 32 chunk (rows rg0.., columns c0.. of a parameter with
+// `rows` x `cols`) is already staged in `buf`; each store instruction writes 8
+// rows x 64 bytes (16 bytes per lane), so every 32-byte sector is written
+// whole.
+DM_DEV void store_final_chunk(const GemmArgs& g, const Bucket& B, const TileInfo& T, int rg0,
+                              int c0, int rows, int cols, uint32_t buf, int lane) {
   const InternalMat im = g.imat[B.first + T.mat];
-  __nv_bfloat16* row = g.packed + im.packed_off + (long long)r * cols;
-  if ((cols & 7) == 0 && c0 + 32 <= cols) {
-    store_bf16x32(row + c0, o);
-  } else {
+  __nv_bfloat16* P = g.packed + im.packed_off;
+  const bool vec = (cols & 7) == 0 && c0 + 32 <= cols;
+  const int u = lane & 3;  // 16-byte unit of the row
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (c0 + j < cols) row[c0 + j] = __float2bfloat16_rn(o[j]);
+  for (int it = 0; it < 4; ++it) {
+    const int row = it * 8 + (lane >> 2);
+    const int r = rg0 + row;
+    if (r >= rows) continue;
+    uint32_t w[4];
+    ld_shared_v4(buf + epi_off(row, u), w[0], w[1], w[2], w[3]);
+    __nv_bfloat16* dst = P + (long long)r * cols + c0 + u * 8;
+    if (vec) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(w);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (c0 + u * 8 + k < cols) dst[k] = e[k];
+    }
   }
 }
 
@@ -457,7 +443,9 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
             bulk_commit();
           }
         } else {
-          if (r < nrows) store_final_chunk(g, B, T, r, c0, ncols, o);
+          epi_store_row(buf(b), lane, o);
+          __syncwarp();
+          store_final_chunk(g, B, T, rg0, c0, nrows, ncols, buf(b), lane);
           __syncwarp();  // every lane is done reading buffer b
         }
         // operand of chunk cc + 2 into the buffer just used
@@ -467,16 +455,26 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
         }
       } else {
         const int m = B.m;
+        // both buffers free of earlier stores
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
         if (g.beta != 0.f) {
-          float a[32];
-          if (r < m) {
-            load_bf16x32(B.slot[g.sAux] + (long long)T.mat * B.stride_m +
-                             (long long)r * B.pitch_m + c0,
-                         a);
-          } else {
+          // beta*A: the 32 x 32 chunk of A comes in with 8 rows x 64 bytes per
+          // load instruction through buffer 1, then each lane takes its row
+          const __nv_bfloat16* A = B.slot[g.sAux] + (long long)T.mat * B.stride_m + c0;
+          const int u = lane & 3;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a[j] = 0.f;
+          for (int it = 0; it < 4; ++it) {
+            const int row = it * 8 + (lane >> 2);
+            uint4 q = make_uint4(0u, 0u, 0u, 0u);
+            if (rg0 + row < m)
+              q = *reinterpret_cast<const uint4*>(A + (long long)(rg0 + row) * B.pitch_m + u * 8);
+            st_shared_v4(buf(1) + epi_off(row, u), q.x, q.y, q.z, q.w);
           }
+          __syncwarp();
+          float a[32];
+          epi_load_row(buf(1), lane, a);
+          __syncwarp();  // buffer 1 is rewritten below
 #pragma unroll
           for (int j = 0; j < 32; ++j) o[j] = fmaf(g.gamma, v[j], g.beta * a[j]);
         } else {
@@ -489,9 +487,6 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
           for (int j = 0; j < 32; ++j)
             if (j == d) o[j] += alpha;
         }
-        // both buffers free of earlier stores
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
         const bool diag_chunk = diag_tile && c_loc == r_loc;
         epi_store_row(buf(0), lane, o);
         if (diag_chunk) {
