@@ -121,7 +121,7 @@ def run_ns(dm, ps, steps, variant=0, abc=None):
 
 
 # ------------------------------------------------------------------ NS
-@pytest.mark.parametrize("steps", [0, 1, 5])
+@pytest.mark.parametrize("steps", [0, 1, 2, 5, 8])
 def test_ns_batched_odd_shapes(dm, wl, steps):
     ps = PackedSet(dm, ODD_SHAPES)
     ins = []
@@ -135,6 +135,30 @@ def test_ns_batched_odd_shapes(dm, wl, steps):
         ref = oracle.newton_schulz(ins[i], steps)
         err = rel(np64(ps.view(i)), ref)
         assert err <= NS_TOL[steps], f"{s} steps={steps}: rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("steps", [0, 1])
+def test_ns_eps_is_added_to_the_norm(dm, wl, steps):
+    """With ||U|| ~ 1e-3 and eps = 1e-3, X0 = U / (||U|| + eps) is about half of
+    U / ||U||: the GPU result must follow the oracle with that eps and differ
+    clearly from the default eps."""
+    shapes = [(64, 200), (300, 7), (256, 256)]
+    ps = PackedSet(dm, shapes)
+    ins = []
+    for i, s in enumerate(shapes):
+        u = wl.random_matrix(s, 400 + i, "cuda", 1.0, torch.float32)
+        u = (u / u.norm() * 1e-3).to(torch.bfloat16)
+        ps.view(i).copy_(u)
+        ins.append(np64(u))
+    dm.ns_batched(ps.shapes, ps.packed, ps.offsets, ps.workspace, ns_steps=steps, eps=1e-3,
+                  ws_bytes=ps.ws_bytes)
+    assert dm.stream_status(ps.workspace) == dm.OK
+    for i, s in enumerate(shapes):
+        got = np64(ps.view(i))
+        ref = oracle.newton_schulz(ins[i], steps, eps=1e-3)
+        default = oracle.newton_schulz(ins[i], steps)
+        assert rel(got, ref) <= NS_TOL[steps], f"{s}: rel err {rel(got, ref):.3e}"
+        assert rel(got, default) > 10 * NS_TOL[steps], f"{s}: eps had no effect"
 
 
 def test_ns_phase_isolation(dm, wl):
