@@ -39,6 +39,8 @@
  *  - NaN / Inf in the inputs propagate; nothing is clamped.  An all-zero
  *    gradient gives O = 0, so W is unchanged.
  *  - Calls that share a workspace must not overlap on the GPU.
+ *  - Tensors of one call must not overlap each other (gradients, momenta,
+ *    weights, the packed buffer and the workspace are distinct memory).
  */
 #ifndef DMUON_H
 #define DMUON_H

@@ -31,7 +31,7 @@ CASES = [
     ("llama-3.2-3b", 5, 0, (2, 3, 6)),
     ("llama-3.1-8b", 5, 0, (1, 0, 6)),
     ("qwen2.5-7b", 5, 0, (1, 0)),
-    ("qwen2.5-7b", 5, 1, (1, 2, 6)),
+    ("qwen2.5-7b", 5, 1, (1, 4, 6)),      # k, gate (tall), down
     ("qwen2.5-7b", 3, 1, (1, 6)),
     ("qwen2.5-7b", 8, 0, (1,)),
     ("qwen2.5-7b", 8, 1, (2,)),
