@@ -133,37 +133,35 @@ def traffic_record():
 
 
 # ---------------------------------------------------------------- CPU oracle
-def oracle_sample(workload_name: str, budget_flops: float = 4.5e11):
+def oracle_sample(workload_name: str, ns_steps: int = 5, warm: bool = False):
     """Time the fp64 oracle on a bounded sample of the workload and extrapolate
-    to one full Muon step (5 NS steps, every matrix).
+    to one full Muon step (`ns_steps` NS steps, every matrix).
 
-    The sample is one matrix of each of the cheapest distinct shapes, taken in
-    order of cost until about `budget_flops` nominal fp64 NS flops (1 step), run
-    through momentum, one Newton-Schulz step and the update.  The measured time
-    per NS flop and per element scales the sample to the whole set.
+    The sample is one matrix of every distinct shape of the set -- the large
+    MLP shapes that carry most of the flops included -- each run through
+    momentum, one Newton-Schulz step and the update.  Each shape's own
+    measured NS time scales by its multiplicity and `ns_steps` (one NS step of
+    a shape costs the same every step); momentum and update scale by elements.
+    `warm` runs only the cheapest shape (warm-up of the BLAS threads).
     Returns (ms_per_full_step, description, seconds_spent)."""
     import numpy as np
     import oracle
     from newton_schulz_owner_gb300 import workloads as wl
 
-    def nominal(s, k):   # dense fp64 flops of k NS steps: 4 m^2 n + 2 m^3 per step
+    def nominal(s):   # dense fp64 flops of one NS step: 4 m^2 n + 2 m^3
         m, n = min(s), max(s)
-        return k * (4.0 * m * m * n + 2.0 * m ** 3)
+        return 4.0 * m * m * n + 2.0 * m ** 3
 
     w = wl.WORKLOADS[workload_name]
     shapes = w.shapes()
-    distinct = sorted(set(shapes), key=lambda s: nominal(s, 1))
-    sample, acc = [], 0.0
-    for s in distinct:
-        if sample and acc + nominal(s, 1) > budget_flops:
-            break
-        sample.append(s)
-        acc += nominal(s, 1)
+    distinct = sorted(set(shapes), key=nominal)
+    if warm:
+        distinct = distinct[:1]
     rng = np.random.default_rng(0)
-    t_ns = t_ew = 0.0
-    f_ns = e_ew = 0.0
+    t_ew = e_ew = 0.0
+    t_ns = {}
     t_all = time.perf_counter()
-    for s in sample:
+    for s in distinct:
         G = rng.standard_normal(s) * 1e-3
         M = np.zeros(s)
         W = rng.standard_normal(s) * 0.02
@@ -176,15 +174,16 @@ def oracle_sample(workload_name: str, budget_flops: float = 4.5e11):
         t3 = time.perf_counter()
         t_ew += (t1 - t0) + (t3 - t2)
         e_ew += s[0] * s[1]
-        t_ns += t2 - t1
-        f_ns += nominal(s, 1)
+        t_ns[s] = t2 - t1
     spent = time.perf_counter() - t_all
-    total_s = sum(nominal(s, 5) for s in shapes) * (t_ns / f_ns) + \
+    if warm:
+        return None, "warm-up", spent
+    total_s = sum(t_ns[s] * ns_steps for s in shapes) + \
         sum(r * c for r, c in shapes) * (t_ew / e_ew)
-    desc = (f"fp64 oracle on one matrix of each of {len(sample)} of the {len(distinct)} "
-            f"distinct shapes of {workload_name} ({', '.join(f'{r}x{c}' for r, c in sample)}), "
-            f"1 NS step; scaled to all {len(shapes)} matrices x 5 NS steps by nominal "
-            f"flops (NS) and elements (momentum, update); extrapolated")
+    desc = (f"fp64 oracle, one matrix of each of the {len(distinct)} distinct shapes of "
+            f"{workload_name} ({', '.join(f'{r}x{c}' for r, c in distinct)}), one NS step "
+            f"each, timed directly; extrapolated to all {len(shapes)} matrices x {ns_steps} NS "
+            f"steps by each shape's own time (NS) and by elements (momentum, update)")
     return total_s * 1e3, desc, spent
 
 
@@ -193,20 +192,26 @@ def run_reference(args, rank, world):
         return 0
     cores = os.cpu_count()
     for _ in range(args.warmup):
-        oracle_sample(args.workload)
-    vals = []
+        oracle_sample(args.workload, args.ns_steps, warm=True)
+    vals, spent = [], []
     for _ in range(args.steps):
-        ms, desc, _ = oracle_sample(args.workload)
+        ms, desc, sec = oracle_sample(args.workload, args.ns_steps)
         vals.append(ms)
+        spent.append(sec)
     v = statistics.median(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "ms",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": v,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.workload, "ns_steps": 5,
+        "data": "synthetic", "config": {"workload": args.workload, "ns_steps": args.ns_steps,
                                         "variant": "standard"},
+        "extrapolated": True,
+        "note": "each timed step is a bounded sample (one matrix of every distinct shape, one "
+                "NS step); value is that sample extrapolated to one whole Muon step, not a "
+                "timed whole step",
         "cpu_baseline": {"value": v, "unit": "ms", "cores": cores, "kind": "oracle",
-                         "sample": desc, "blas": blas_name()},
+                         "sample": desc, "blas": blas_name(), "extrapolated": True,
+                         "sample_seconds": statistics.median(spent)},
         "e2e": {"value": v, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -582,9 +587,10 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        cms, desc, _ = oracle_sample(args.workload)
+        cms, desc, sec = oracle_sample(args.workload, args.ns_steps)
         line["cpu_baseline"] = {"value": cms, "unit": "ms", "cores": os.cpu_count(),
-                                "kind": "oracle", "sample": desc, "blas": blas_name()}
+                                "kind": "oracle", "sample": desc, "blas": blas_name(),
+                                "extrapolated": True, "sample_seconds": sec}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

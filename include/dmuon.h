@@ -6,8 +6,8 @@
  * owner of a set of 2-D projection matrices runs, once per step,
  *   1. Nesterov momentum on each gradient and packs the result (bf16) into one
  *      contiguous per-owner buffer;
- *   2. one Newton-Schulz orthogonalisation of every packed matrix
- *      ("One owner. One Newton-Schulz.");
+ *   2. one Newton-Schulz orthogonalisation of every packed matrix (home page,
+ *      owner section: each matrix is orthogonalised once, by its owner);
  *   3. the scaled weight update.
  * The pages name Muon and Newton-Schulz but do not write them out; the library
  * uses the standard Muon forms:
@@ -165,10 +165,14 @@ int dmuon_unpack_update(int n, const dmuon_shape* shp, void* const* weight,
  * the tensor-core products: it visits the shape groups smallest first, and
  * while one group is orthogonalised the later groups are packed and relaid
  * out and the earlier groups' weights are updated, so that only the first
- * group's pack and the last group's update run alone.  That work runs on a lowest-priority
- * stream the library creates once per device, ordered against `stream` with
- * events; when the call returns, all of it is ordered before any later work
- * on `stream`.  Results are identical to the three separate calls.
+ * group's pack and the last group's update run alone.  That work runs on a
+ * lowest-priority companion stream that the library creates for `stream` on
+ * its first call with it (one per caller stream, up to 16 per device; past
+ * that, and while `stream` is being captured, a companion shared by the device
+ * serves), ordered against `stream` with events; when the call returns, all of
+ * it is ordered before any later work on `stream`.  Owners that step on
+ * different caller streams therefore run concurrently.  Results are identical
+ * to the three separate calls.
  * The call can be captured into a CUDA graph (stream capture on `stream`) and
  * replayed: its tables are written by a kernel, and the second stream joins
  * the capture through the events.  Make one call on the device before the
@@ -183,7 +187,7 @@ int dmuon_muon_step(int n, const dmuon_shape* shp, const void* const* grad, int 
 
 /*
  * dmuon_adamw -- AdamW step for the parameters Muon does not own (home page,
- * "LLM Pretraining": dmuon.Muon(..., adamw_lr=1e-3); "VLA and VLM":
+ * "LLM Pretraining": AdamW learning rate 1e-3 in the usage example; "VLA and VLM":
  * embeddings, norms and heads stay outside the Muon set).  The pages give only
  * the learning rate; the update is the usual AdamW with decoupled weight decay:
  *   p <- p * (1 - lr*wd)
@@ -224,7 +228,9 @@ int dmuon_stream_status(cudaStream_t stream, void* workspace);
  * one block that waits on a shared-memory barrier nobody signals, with a
  * limit of `budget_us` microseconds (1..1000000).  The wait gives up, the
  * kernel records DMUON_ERR_TIMEOUT in the workspace error word and returns,
- * leaving the context usable.  Needs ws_bytes >= 256.
+ * leaving the context usable.  Needs ws_bytes >= 256.  workspace == NULL
+ * targets the error word of the built-in scratch array of
+ * dmuon_ns_batched_noalloc instead (read it with dmuon_noalloc_status).
  */
 int dmuon_debug_wait_timeout(void* workspace, size_t ws_bytes, int budget_us,
                              cudaStream_t stream);
@@ -258,13 +264,27 @@ int dmuon_debug_wait_timeout(void* workspace, size_t ws_bytes, int budget_us,
  *  - Sharing: every call on a device uses the same array, which keeps the last
  *    call's contents.  Calls whose work overlaps on the GPU (two streams, two
  *    host threads without ordering) race on it and give wrong results; order
- *    them on one stream.  Each call clears the array's device error word when
- *    it starts; a bounded wait that gives up inside this call leaves the
- *    outputs incomplete and is not reported to the caller.
+ *    them on one stream.
+ *  - Failures: the array holds its own device error word.  Each call clears it
+ *    when it starts; a bounded wait that gives up inside the call leaves the
+ *    outputs incomplete and records DMUON_ERR_TIMEOUT there, which
+ *    dmuon_noalloc_status reports.  Read it before the next call.
  */
 int dmuon_ns_batched_noalloc(int n, const dmuon_shape* shp, void* packed_bf16,
                              const int64_t* offset, int ns_steps, int ns_variant,
                              const float* abc, float eps, cudaStream_t stream);
+
+/*
+ * dmuon_noalloc_status -- dmuon_stream_status for the built-in scratch array
+ * of dmuon_ns_batched_noalloc on the current device: synchronises `stream`,
+ * then reports (and clears) the array's device error word: DMUON_OK,
+ * DMUON_ERR_TIMEOUT when a bounded wait inside a call gave up, DMUON_ERR_CUDA
+ * when the stream holds a CUDA error.  Like the call itself it allocates
+ * nothing; on a device where no call has run yet it first looks up the
+ * array's address (the same one-time set-up).  The DMuon pages have no
+ * counterpart to it.
+ */
+int dmuon_noalloc_status(cudaStream_t stream);
 
 /* Human-readable text for a status code (static storage). */
 const char* dmuon_status_string(int status);

@@ -240,10 +240,27 @@ struct DevInfo {
   int max_clusters = 0;  // resident CTA pairs of the product kernel
   // Lowest-priority stream on which a whole step runs its memory-bound kernels
   // next to the products (null: the step runs on the caller's stream alone).
+  // This one serves callers whose stream is being captured and callers beyond
+  // the per-stream table below.
   cudaStream_t aux = nullptr;
 };
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
+
+// Each caller stream gets its own lowest-priority companion stream (up to
+// kAuxPerDevice caller streams per device), so that owners stepping on
+// different caller streams do not queue behind each other's memory-bound work.
+// Past that many streams, or while the caller's stream is being captured into
+// a graph (no stream is created then), the device's shared companion serves;
+// sharing it serialises that work but never changes a result, since every
+// piece of it is ordered against its own caller stream by events.
+constexpr int kAuxPerDevice = 16;
+struct AuxEntry {
+  cudaStream_t caller = nullptr;
+  cudaStream_t aux = nullptr;
+};
+AuxEntry g_aux[kMaxDevices][kAuxPerDevice];
+int g_aux_used[kMaxDevices] = {};
 
 int device_info(DevInfo* out) {
   int d = 0;
@@ -274,6 +291,33 @@ int device_info(DevInfo* out) {
   }
   *out = D;
   return D.status;
+}
+
+// Companion stream of `caller` on the current device (D from device_info).
+cudaStream_t aux_stream_for(const DevInfo& D, cudaStream_t caller) {
+  if (D.aux == nullptr) return nullptr;
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return D.aux;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int k = 0; k < g_aux_used[d]; ++k)
+    if (g_aux[d][k].caller == caller) return g_aux[d][k].aux;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(caller, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+    (void)cudaGetLastError();
+    return D.aux;
+  }
+  if (g_aux_used[d] >= kAuxPerDevice) return D.aux;
+  int least = 0, greatest = 0;
+  cudaStream_t x = nullptr;
+  if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&x, cudaStreamNonBlocking, least) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return D.aux;
+  }
+  g_aux[d][g_aux_used[d]].caller = caller;
+  g_aux[d][g_aux_used[d]].aux = x;
+  ++g_aux_used[d];
+  return x;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -657,7 +701,7 @@ int run(const Request& R) {
     });
     EventSet ev;  // [0, nb): mb(k) done; [nb, 2nb): NS(k) done; 2nb: aux done
     if (!ev.create(2 * nb + 1)) return DMUON_ERR_CUDA;
-    cudaStream_t x = D.aux;
+    cudaStream_t x = aux_stream_for(D, s);
     auto mb = [&](int k, cudaStream_t st) {
       const EwRange r = range_of(ord[k], ord[k] + 1);
       return launch_momentum_pack(r, gbf16, R.beta, packed, partials, st) == cudaSuccess &&
@@ -779,6 +823,12 @@ int dmuon_ns_batched_noalloc(int n, const dmuon_shape* shp, void* packed_bf16,
   // is written before it is read
   if (cudaMemsetAsync(scratch, 0, sizeof(int), stream) != cudaSuccess) return DMUON_ERR_CUDA;
   return run(R);
+}
+
+int dmuon_noalloc_status(cudaStream_t stream) {
+  void* scratch = noalloc_scratch();
+  if (scratch == nullptr) return DMUON_ERR_CUDA;
+  return dmuon_stream_status(stream, scratch);
 }
 
 int dmuon_plan(int n, const dmuon_shape* shp, int n_owners, int* owner_of, int64_t* offset,
@@ -962,7 +1012,13 @@ int dmuon_stream_status(cudaStream_t stream, void* workspace) {
 
 int dmuon_debug_wait_timeout(void* workspace, size_t ws_bytes, int budget_us,
                              cudaStream_t stream) {
-  if (workspace == nullptr || ws_bytes < kHdrBytes) return DMUON_ERR_INVALID_ARG;
+  if (workspace == nullptr) {
+    // the error word of dmuon_ns_batched_noalloc's built-in scratch
+    workspace = noalloc_scratch();
+    if (workspace == nullptr) return DMUON_ERR_CUDA;
+    ws_bytes = DMUON_NOALLOC_SCRATCH_BYTES;
+  }
+  if (ws_bytes < kHdrBytes) return DMUON_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return DMUON_ERR_ALIGNMENT;
   if (budget_us < 1 || budget_us > 1000000) return DMUON_ERR_INVALID_ARG;
   DevInfo D;

@@ -28,7 +28,8 @@ DEFAULT_ABC = (3.4445, -4.7750, 2.0315)
 
 EXPORTED = ("dmuon_plan", "dmuon_workspace_bytes", "dmuon_pack", "dmuon_ns_batched",
             "dmuon_unpack_update", "dmuon_muon_step", "dmuon_stream_status",
-            "dmuon_debug_wait_timeout", "dmuon_ns_batched_noalloc", "dmuon_adamw",
+            "dmuon_debug_wait_timeout", "dmuon_ns_batched_noalloc", "dmuon_noalloc_status",
+            "dmuon_adamw",
             "dmuon_adamw_workspace_bytes", "dmuon_status_string", "dmuon_version",
             "dmuon_launch_count")
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -60,6 +61,8 @@ _lib.dmuon_muon_step.restype = _i
 _lib.dmuon_ns_batched_noalloc.argtypes = [_i, _ShapeP, _vp, _i64p, _i, _i,
                                           ctypes.POINTER(ctypes.c_float), _f, _vp]
 _lib.dmuon_ns_batched_noalloc.restype = _i
+_lib.dmuon_noalloc_status.argtypes = [_vp]
+_lib.dmuon_noalloc_status.restype = _i
 _lib.dmuon_adamw_workspace_bytes.argtypes = [_i]
 _lib.dmuon_adamw_workspace_bytes.restype = _sz
 _d = ctypes.c_double
@@ -197,6 +200,12 @@ def ns_batched_noalloc(shapes, packed, offsets, ns_steps: int = 5, variant: int 
            "dmuon_ns_batched_noalloc")
 
 
+def noalloc_status(stream=None) -> int:
+    """Synchronise the stream and report (and clear) the error word of the
+    built-in scratch array used by :func:`ns_batched_noalloc`."""
+    return int(_lib.dmuon_noalloc_status(_stream(stream)))
+
+
 def unpack_update(shapes, weights, lr, packed, offsets, workspace, stream=None) -> None:
     n = len(shapes)
     wdt = _dtype(weights[0]) if n else BF16
@@ -241,8 +250,12 @@ def stream_status(workspace=None, stream=None) -> int:
 
 
 def debug_wait_timeout(workspace, budget_us: int, stream=None) -> None:
-    _check(_lib.dmuon_debug_wait_timeout(_addr(workspace), workspace.numel(), int(budget_us),
-                                         _stream(stream)), "dmuon_debug_wait_timeout")
+    """Make a bounded device wait run out; workspace None targets the built-in
+    scratch array of :func:`ns_batched_noalloc`."""
+    ws = None if workspace is None else _addr(workspace)
+    nbytes = 0 if workspace is None else workspace.numel()
+    _check(_lib.dmuon_debug_wait_timeout(ws, nbytes, int(budget_us), _stream(stream)),
+           "dmuon_debug_wait_timeout")
 
 
 class MuonOwner:

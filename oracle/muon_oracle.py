@@ -11,8 +11,8 @@ What it computes, and where that comes from
 DMuon home page ("DMuon", sections "What DMuon Can Do" / "LLM Pretraining"):
 each 2-D projection parameter has one owner; the owner runs Muon for it --
 momentum, one Newton-Schulz orthogonalisation, update -- once per step
-("One owner. One Newton-Schulz."), with the API knobs ``lr=0.02`` and
-``ns_steps=5``.  "Z2 vs Z3 Modes" ("The two packed-buffer lifecycles"): all
+(owner section: each matrix is orthogonalised once, by its owner), with a
+learning rate of 0.02 and 5 Newton-Schulz steps in the usage example.  "Z2 vs Z3 Modes" ("The two packed-buffer lifecycles"): all
 Muon-target matrices that share an owner sit in one contiguous buffer.
 
 The pages name Muon and Newton-Schulz but never write the formulas.  The
@@ -53,13 +53,13 @@ import numpy as np
 # Standard Muon quintic coefficients (a, b, c) and normalisation epsilon.
 NS_COEFFS: Tuple[float, float, float] = (3.4445, -4.7750, 2.0315)
 NS_EPS: float = 1e-7
-# Home page, "LLM Pretraining" code example: Muon(model, lr=0.02, ns_steps=5, ...).
+# Home page, "LLM Pretraining" usage example: learning rate 0.02, 5 Newton-Schulz steps.
 DEFAULT_LR: float = 0.02
 DEFAULT_NS_STEPS: int = 5
 DEFAULT_BETA: float = 0.95
 
 # Packed-segment alignment: 256 bytes (= 128 bf16 elements).  "Z2 vs Z3 Modes",
-# "The two packed-buffer lifecycles", only says "a single contiguous buffer";
+# "The two packed-buffer lifecycles", only says that they share one contiguous buffer;
 # the alignment is this library's reading so that every segment can be read
 # with 16-byte vector loads and TMA.
 PACK_ALIGN_BYTES: int = 256
@@ -103,8 +103,8 @@ def newton_schulz(U: np.ndarray, ns_steps: int = DEFAULT_NS_STEPS,
                   abc: Sequence[float] = NS_COEFFS, eps: float = NS_EPS) -> np.ndarray:
     """Standard quintic Newton-Schulz orthogonalisation of one matrix (fp64).
 
-    Home page: "One owner. One Newton-Schulz." -- run once per matrix with the
-    ``ns_steps`` knob of the Muon API.  Steps in the iteration's own order:
+    Home page, owner section: each matrix is orthogonalised once per step, by
+    its owner, with the number of steps as an optimizer argument.  Steps in the iteration's own order:
     transpose-if-tall, normalise, then ``ns_steps`` times A = X X^T,
     B = b A + c A A, X = a X + B X; undo the transpose.
     """
@@ -173,7 +173,7 @@ def muon_step(G: np.ndarray, M: np.ndarray, W: np.ndarray, lr: float = DEFAULT_L
 # ---------------------------------------------------------------------------
 # AdamW for the parameters Muon does not own
 # ---------------------------------------------------------------------------
-ADAMW_DEFAULT_LR = 1e-3          # home page, "LLM Pretraining": Muon(..., adamw_lr=1e-3)
+ADAMW_DEFAULT_LR = 1e-3          # home page, "LLM Pretraining": AdamW learning rate in the usage example
 ADAMW_DEFAULT_BETAS = (0.9, 0.999)
 ADAMW_DEFAULT_EPS = 1e-8
 ADAMW_DEFAULT_WD = 0.01
@@ -186,7 +186,7 @@ def adamw_step(p: np.ndarray, g: np.ndarray, m: np.ndarray, v: np.ndarray, step:
     """One AdamW step (decoupled weight decay), fp64.  Returns (p, m, v).
 
     Home page, "LLM Pretraining": parameters outside the Muon set (embeddings,
-    norms, heads) use AdamW with ``adamw_lr``.  The pages give no other
+    norms, heads) use AdamW with its own learning rate.  The pages give no other
     hyper-parameter; the reading is the usual AdamW with decay applied to the
     parameter before the moment update:
       p <- p (1 - lr wd)

@@ -6,6 +6,8 @@ lie in the quintic's singular-value band (a property that holds at any size).
 
 Sample choice keeps the fp64 oracle to seconds per matrix: small k/v
 matrices, one square q, and one of the large MLP matrices."""
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -55,8 +57,10 @@ def test_full_set_sampled_against_oracle(name, ns_steps, variant, projs):
     W = wl.alloc_flat(shapes, w.weight_dtype, dev)
     wl.fill_grads(w, G, step=0)
     wl.fill_weights(w, W)
-    rng = np.random.default_rng(abs(hash((name, ns_steps, variant))) % 2 ** 31)
+    # a stable digest of the case picks the layer, so every run checks the same matrices
+    rng = np.random.default_rng(zlib.crc32(f"{name}/{ns_steps}/{variant}".encode()))
     sample = [int(rng.integers(0, w.layers)) * 7 + p for p in projs]
+    where = f"{name} ns_steps={ns_steps} variant={variant} sample={sample}"
     w0 = {i: np64(W.views[i]) for i in sample}
     g0 = {i: np64(G.views[i]) for i in sample}
     owner.step(G.views, M.views, W.views, lr=0.02, beta=0.95, ns_steps=ns_steps)
@@ -67,9 +71,9 @@ def test_full_set_sampled_against_oracle(name, ns_steps, variant, projs):
         m_ref, o_ref, w_ref = oracle.muon_step(g0[i], np.zeros(s), w0[i], lr=0.02, beta=0.95,
                                                ns_steps=ns_steps,
                                                variant="gram" if gram else "standard")
-        assert rel(np64(M.views[i]), m_ref) <= 1e-5, f"momentum {i} {s}"
+        assert rel(np64(M.views[i]), m_ref) <= 1e-5, f"momentum #{i} {s} ({where})"
         err_o = rel(np64(owner.packed_view(i)), o_ref)
-        assert err_o <= NS_TOL[ns_steps], f"O {name} #{i} {s}: {err_o:.3e}"
+        assert err_o <= NS_TOL[ns_steps], f"O #{i} {s}: {err_o:.3e} ({where})"
         # bf16 weights: W' - W'_64 = (bf16 rounding of the result) + lr*s*(O_64 - O),
         # so its norm is bounded by the rounding residual of RNE(W'_64) (same
         # statistics, 25% slack) plus the NS tolerance on the update itself
@@ -77,9 +81,9 @@ def test_full_set_sampled_against_oracle(name, ns_steps, variant, projs):
         resid = np.linalg.norm(oracle.round_bf16(w_ref) - w_ref)
         bound = 1.25 * resid + NS_TOL[ns_steps] * np.linalg.norm(w_ref - w0[i])
         err_w = np.linalg.norm(w_gpu - w_ref)
-        assert err_w <= bound, f"W {name} #{i} {s}: {err_w:.3e} > {bound:.3e}"
+        assert err_w <= bound, f"W #{i} {s}: {err_w:.3e} > {bound:.3e} ({where})"
         sv = torch.linalg.svdvals(owner.packed_view(i).float()).cpu().numpy()
-        assert sv.max() <= 1.2025 * 1.02
+        assert sv.max() <= 1.2025 * 1.02, f"band #{i} {s}: {sv.max():.4f} ({where})"
     if w.n_owners > 1:   # owner buffers: every matrix lives inside its owner's buffer
         starts = np.cumsum([0] + owner.owner_elems[:-1])
         for i, (r, c) in enumerate(shapes):
