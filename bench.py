@@ -132,6 +132,23 @@ def traffic_record():
     return d
 
 
+def ns_flops(shapes, ns_steps: int) -> float:
+    """Algorithmic flops of the standard iteration: per step X X^T (m^2 n,
+    symmetric, counted half), A A (m^3, half) and B X (2 m^2 n)."""
+    return float(sum((3.0 * min(s) ** 2 * max(s) + float(min(s)) ** 3) * ns_steps
+                     for s in shapes))
+
+
+def gram_flops(shapes, ns_steps: int) -> float:
+    """Algorithmic flops of the Gram iteration: A0 = X0 X0^T (m^2 n, half) and
+    O = Q X0 (2 m^2 n), and per step the symmetric m^3 products A A, P Q (not
+    at the first step, where Q = P), P P and A P^2 (not at the last step)."""
+    if ns_steps <= 0:
+        return 0.0
+    per = 4 * ns_steps - 3          # m^3 products over the whole iteration
+    return float(sum(3.0 * min(s) ** 2 * max(s) + per * float(min(s)) ** 3 for s in shapes))
+
+
 # ---------------------------------------------------------------- CPU oracle
 def oracle_sample(workload_name: str, ns_steps: int = 5, warm: bool = False):
     """Time the fp64 oracle on a bounded sample of the workload and extrapolate
@@ -185,6 +202,166 @@ def oracle_sample(workload_name: str, ns_steps: int = 5, warm: bool = False):
             f"each, timed directly; extrapolated to all {len(shapes)} matrices x {ns_steps} NS "
             f"steps by each shape's own time (NS) and by elements (momentum, update)")
     return total_s * 1e3, desc, spent
+
+
+def trace_summary(rec, step_ms: float):
+    """Where the CTA pairs of the product kernel spend one traced step.
+
+    `rec` holds one record per CTA of every product launch of the step
+    (dmuon_trace_begin).  Pair time over the product window (first product
+    entry to last product exit) splits into MMA-active (a pair's first MMA
+    issue to its last MMA completion, per launch), fill/drain (resident but
+    before its first or after its last MMA) and not resident (launch gaps,
+    last-wave tails, pairs without a tile).  A whole-step persistent kernel
+    could recover at most the last two."""
+    lead = rec["cta"] % 2 == 0
+    entry, exit_ = rec["t_entry"], rec["t_exit"]
+    t0, t1 = int(entry.min()), int(exit_.max())
+    window = (t1 - t0) * 1e-6
+    pairs = int(rec["cta"].max().item()) // 2 + 1   # pairs of the widest launch
+    has = lead & (rec["t_mma_first"] > 0)
+    busy = float((rec["t_mma_last"][has] - rec["t_mma_first"][has]).sum().item()) * 1e-6
+    resident = float((exit_[lead] - entry[lead]).sum().item()) * 1e-6
+    total = pairs * window
+    launches = sorted(set(rec["launch"].tolist()))
+    spans = []
+    for L in launches:
+        m = rec["launch"] == L
+        spans.append((int(entry[m].min()), int(exit_[m].max())))
+    gaps = sum(max(0, spans[k + 1][0] - spans[k][1]) for k in range(len(spans) - 1)) * 1e-6
+    return {"launches": len(launches), "pairs": pairs, "step_ms": step_ms,
+            "product_window_ms": window,
+            "mma_active_frac": busy / total, "fill_drain_frac": (resident - busy) / total,
+            "not_resident_frac": (total - resident) / total,
+            "launch_gaps_ms": gaps,
+            "recoverable_ms_upper_bound": (total - busy) / pairs,
+            "note": "pair time over the product window of one traced dmuon_muon_step: MMA-active "
+                    "(first MMA issue to last MMA completion of each pair and launch), fill/drain "
+                    "(resident, outside that span), not resident (launch gaps, last-wave tails, "
+                    "pairs without a tile); a whole-step persistent kernel could recover at most "
+                    "the time outside MMA-active"}
+
+
+def owner_times(dmuon, shapes, owner, variant, ns_steps, stream, barrier, grouped_ns_ms):
+    """Each LPT owner's Newton-Schulz as its own call on its segments of the
+    packed buffer, back to back, against all owners in one grouped call: the
+    single-GPU picture of the pages' balanced ownership (the slowest owner
+    bounds a distributed step)."""
+    import torch
+    n = len(shapes)
+    n_owners = max(owner.owner_of) + 1
+    groups = [[i for i in range(n) if owner.owner_of[i] == k] for k in range(n_owners)]
+    groups = [gk for gk in groups if gk]
+    ws_max = max(dmuon.workspace_bytes([shapes[i] for i in gk], variant) for gk in groups)
+    ws_o = torch.zeros(ws_max, dtype=torch.uint8, device=owner.packed.device)
+
+    def owner_ns(gk):
+        dmuon.ns_batched([shapes[i] for i in gk], owner.packed, [owner.offsets[i] for i in gk],
+                         ws_o, ns_steps=ns_steps, variant=variant, stream=stream)
+
+    for gk in groups:
+        owner_ns(gk)
+    barrier()
+    oev = [torch.cuda.Event(enable_timing=True) for _ in range(len(groups) + 1)]
+    with torch.cuda.stream(stream):
+        oev[0].record(stream)
+        for k, gk in enumerate(groups):
+            owner_ns(gk)
+            oev[k + 1].record(stream)
+    barrier()
+    st = dmuon.stream_status(ws_o, stream)
+    if st != dmuon.OK:
+        raise RuntimeError(f"per-owner NS failed: {dmuon.status_string(st)}")
+    o_ms = [oev[k].elapsed_time(oev[k + 1]) for k in range(len(groups))]
+    o_elems = [sum(shapes[i][0] * shapes[i][1] for i in gk) for gk in groups]
+    return {"n_owners": len(groups), "ns_ms": o_ms, "elements": o_elems,
+            "back_to_back_ms": sum(o_ms), "grouped_ns_ms": grouped_ns_ms,
+            "max_over_mean": max(o_ms) / (sum(o_ms) / len(o_ms)),
+            "note": "each owner's Newton-Schulz alone (norms from the packed values), "
+                    "back to back, vs all owners in one grouped call"}
+
+
+# The benchmark's other projection-set configurations, measured after the main
+# workload when it runs at its default: (workload, variant, ns_steps).
+OTHER_CONFIGS = [("single-256x1024", 0, 5), ("qwen2.5-1.5b", 0, 5), ("llama-3.2-3b", 0, 5),
+                 ("qwen2.5-7b", 0, 3), ("qwen2.5-7b", 1, 3), ("qwen2.5-7b", 0, 5),
+                 ("qwen2.5-7b", 1, 5), ("qwen2.5-7b", 0, 8), ("qwen2.5-7b", 1, 8)]
+
+
+def config_point(dmuon, wl, name, variant, ns_steps, dev, gpu_index, peak, steps=3, warmup=3):
+    """One configuration, measured like the main workload but shorter: the whole
+    step through dmuon_muon_step (median of `steps`), then the same step as
+    three calls with events between them for the Newton-Schulz phase; per-owner
+    times where the set has an owner partition.  Clocks sampled throughout."""
+    import torch
+    w = wl.WORKLOADS[name]
+    shapes = w.shapes()
+    owner = dmuon.MuonOwner(shapes, n_owners=w.n_owners, variant=variant, device=dev)
+    G = wl.alloc_flat(shapes, w.grad_dtype, dev)
+    M = wl.alloc_flat(shapes, torch.float32, dev)
+    W = wl.alloc_flat(shapes, w.weight_dtype, dev)
+    wl.fill_grads(w, G, step=0)
+    wl.fill_weights(w, W)
+    stream = torch.cuda.Stream(device=dev)
+    gs = [s for s in shapes if dmuon.ns_variant_for(s, ns_steps, variant) == 1]
+    ss = [s for s in shapes if dmuon.ns_variant_for(s, ns_steps, variant) != 1]
+    flops = gram_flops(gs, ns_steps) + ns_flops(ss, ns_steps)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+
+    def step():
+        owner.step(G.views, M.views, W.views, lr=0.02, beta=0.95, ns_steps=ns_steps,
+                   stream=stream)
+
+    for _ in range(warmup):
+        step()
+    barrier()
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for k in range(steps):
+        step()
+        ev[k + 1].record(stream)
+    barrier()
+    ph = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for k in range(steps):
+            ph[k][0].record(stream)
+            dmuon.pack(shapes, G.views, M.views, 0.95, owner.packed, owner.offsets,
+                       owner.workspace, stream=stream)
+            ph[k][1].record(stream)
+            dmuon.ns_batched(shapes, owner.packed, owner.offsets, owner.workspace,
+                             ns_steps=ns_steps, variant=variant, use_pack_norms=True,
+                             stream=stream)
+            ph[k][2].record(stream)
+            dmuon.unpack_update(shapes, W.views, 0.02, owner.packed, owner.offsets,
+                                owner.workspace, stream=stream)
+            ph[k][3].record(stream)
+    barrier()
+    clocks = sampler.stop()
+    st = dmuon.stream_status(owner.workspace, stream)
+    if st != dmuon.OK:
+        raise RuntimeError(f"{name}: {dmuon.status_string(st)}")
+    step_ms = statistics.median(ev[k].elapsed_time(ev[k + 1]) for k in range(steps))
+    ns_ms = statistics.median(p[1].elapsed_time(p[2]) for p in ph)
+    out = {"workload": name, "variant": {0: "standard", 1: "gram", 2: "gram-all"}[variant],
+           "ns_steps": ns_steps, "matrices": len(shapes),
+           "gram_matrices": len(gs), "step_ms": step_ms, "ns_ms": ns_ms,
+           "pack_ms": statistics.median(p[0].elapsed_time(p[1]) for p in ph),
+           "update_ms": statistics.median(p[2].elapsed_time(p[3]) for p in ph),
+           "ns_tflops_algorithmic": flops / (ns_ms * 1e-3) / 1e12,
+           "ns_frac_of_peak": flops / (ns_ms * 1e-3) / 1e12 / peak,
+           "matrices_per_s": len(shapes) / (step_ms * 1e-3), "steps": steps, "warmup": warmup,
+           "clocks": clocks}
+    if w.n_owners > 1:
+        out["owners"] = owner_times(dmuon, shapes, owner, variant, ns_steps, stream, barrier,
+                                    ns_ms)
+    del owner, G, M, W
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_reference(args, rank, world):
@@ -246,7 +423,6 @@ def run_gpu(args, rank, world, local_rank):
         build_lib.build()
     from newton_schulz_owner_gb300 import dmuon
     from newton_schulz_owner_gb300 import workloads as wl
-    import oracle
 
     dist = None
     if world > 1:
@@ -267,13 +443,10 @@ def run_gpu(args, rank, world, local_rank):
     wl.fill_grads(w, G, step=0)
     wl.fill_weights(w, W)
     stream = torch.cuda.Stream(device=dev)
-    ns_flops = (oracle.gram_ns_flops_algorithmic if args.variant == 1 else
-                oracle.ns_flops_algorithmic)(shapes, args.ns_steps)
-    if args.variant == 1:  # Gram only where n >= 2m; the rest run the standard form
-        gs = [s for s in shapes if max(s) >= 2 * min(s)]
-        ss = [s for s in shapes if max(s) < 2 * min(s)]
-        ns_flops = oracle.gram_ns_flops_algorithmic(gs, args.ns_steps) + \
-            oracle.ns_flops_algorithmic(ss, args.ns_steps)
+    # Gram where the library's rule admits it; the standard form on the rest
+    gs = [s for s in shapes if dmuon.ns_variant_for(s, args.ns_steps, args.variant) == 1]
+    ss = [s for s in shapes if dmuon.ns_variant_for(s, args.ns_steps, args.variant) != 1]
+    flops = gram_flops(gs, args.ns_steps) + ns_flops(ss, args.ns_steps)
     elems = sum(r * c for r, c in shapes)
 
     def step_phases(ev=None):
@@ -343,7 +516,39 @@ def run_gpu(args, rank, world, local_rank):
     t_total = max_over_ranks(sum(step_ms), dist, dev)
     ms = t_total / args.steps
     ns_mean = sum(ns_ms) / len(ns_ms)
-    achieved_tflops = ns_flops / (ns_mean * 1e-3) / 1e12
+    achieved_tflops = flops / (ns_mean * 1e-3) / 1e12
+
+    # ---- one more dmuon_muon_step, outside the timed regions, with the
+    # product launches traced (per-CTA timestamps): what a whole-step
+    # persistent kernel could recover at most
+    ns_trace = None
+    if not args.no_trace:
+        tbuf = torch.zeros(4 << 20, dtype=torch.uint8, device=dev)
+        ns_trace, raw = {}, {}
+        # the whole step (the value's call), then its Newton-Schulz phase alone
+        for label, fn in (("whole_step", whole_step),
+                          ("ns_phase_alone", lambda: dmuon.ns_batched(
+                              shapes, owner.packed, owner.offsets, owner.workspace,
+                              ns_steps=args.ns_steps, variant=args.variant, stream=stream))):
+            te = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            barrier()
+            dmuon.trace_begin(tbuf)
+            te[0].record(stream)
+            fn()
+            te[1].record(stream)
+            barrier()
+            rec = dmuon.trace_end(tbuf)
+            st = dmuon.stream_status(owner.workspace, stream)
+            if st != dmuon.OK:
+                raise RuntimeError(f"traced step failed: {dmuon.status_string(st)}")
+            if rec["cta"].numel():
+                ns_trace[label] = trace_summary(rec, te[0].elapsed_time(te[1]))
+                raw[label] = {k: v.numpy() for k, v in rec.items()}
+        if args.trace_out:
+            import numpy as np
+            np.savez(args.trace_out, **{f"{lab}.{k}": v for lab, d in raw.items()
+                                        for k, v in d.items()})
+        del tbuf
 
     # ---- owners (workloads with an LPT owner partition): each owner's
     # Newton-Schulz as its own call on its segments of the packed buffer, back
@@ -351,36 +556,8 @@ def run_gpu(args, rank, world, local_rank):
     # pages' balanced ownership (the slowest owner bounds a distributed step).
     owners = None
     if w.n_owners > 1:
-        groups = [[i for i in range(n) if owner.owner_of[i] == k] for k in range(w.n_owners)]
-        groups = [gk for gk in groups if gk]
-        ws_max = max(dmuon.workspace_bytes([shapes[i] for i in gk], args.variant) for gk in groups)
-        ws_o = torch.zeros(ws_max, dtype=torch.uint8, device=dev)
-
-        def owner_ns(gk):
-            dmuon.ns_batched([shapes[i] for i in gk], owner.packed, [owner.offsets[i] for i in gk],
-                             ws_o, ns_steps=args.ns_steps, variant=args.variant, stream=stream)
-
-        for gk in groups:
-            owner_ns(gk)
-        barrier()
-        oev = [torch.cuda.Event(enable_timing=True) for _ in range(len(groups) + 1)]
-        with torch.cuda.stream(stream):
-            oev[0].record(stream)
-            for k, gk in enumerate(groups):
-                owner_ns(gk)
-                oev[k + 1].record(stream)
-        barrier()
-        st = dmuon.stream_status(ws_o, stream)
-        if st != dmuon.OK:
-            raise RuntimeError(f"per-owner NS failed: {dmuon.status_string(st)}")
-        o_ms = [oev[k].elapsed_time(oev[k + 1]) for k in range(len(groups))]
-        o_elems = [sum(shapes[i][0] * shapes[i][1] for i in gk) for gk in groups]
-        owners = {"n_owners": len(groups), "ns_ms": o_ms, "elements": o_elems,
-                  "back_to_back_ms": sum(o_ms), "grouped_ns_ms": ns_mean,
-                  "max_over_mean": max(o_ms) / (sum(o_ms) / len(o_ms)),
-                  "note": "each owner's Newton-Schulz alone (norms from the packed values), "
-                          "back to back, vs all owners in one grouped call"}
-        del ws_o
+        owners = owner_times(dmuon, shapes, owner, args.variant, args.ns_steps, stream, barrier,
+                             ns_mean)
 
     # ---- AdamW for the parameters outside the Muon set (embedding, head, norms),
     # timed on its own: bf16 parameters and gradients, fp32 moments.
@@ -439,7 +616,7 @@ def run_gpu(args, rank, world, local_rank):
         n_groups = max(1, min(args.e2e_groups, n // per_layer))
         bounds = [round(g_ * (n // per_layer) / n_groups) * per_layer for g_ in range(n_groups)] + [n]
         gsets = [(bounds[j], bounds[j + 1]) for j in range(n_groups) if bounds[j] < bounds[j + 1]]
-        del owner   # the groups' owners take its place
+        owner = None   # the groups' owners take its place
         torch.cuda.empty_cache()
         g_owner = [dmuon.MuonOwner(shapes[i0:i1], n_owners=w.n_owners, variant=args.variant,
                                    device=dev) for i0, i1 in gsets]
@@ -543,7 +720,7 @@ def run_gpu(args, rank, world, local_rank):
                 # A and B each written once and read once (8m^2 bytes), bf16
                 "algorithmic_bytes": None if args.variant != 0 else float(args.ns_steps * sum(
                     6 * min(r, c) * max(r, c) + 8 * min(r, c) ** 2 for r, c in shapes)),
-                "flops_per_step": ns_flops}
+                "flops_per_step": flops}
     elem_bytes = {"pack": (2 if w.grad_dtype == torch.bfloat16 else 4) + 4 + 4 + 2,
                   "update": 2 + 2 * (2 if w.weight_dtype == torch.bfloat16 else 4)}
     pack_mean = sum(pack_ms) / len(pack_ms)
@@ -570,7 +747,7 @@ def run_gpu(args, rank, world, local_rank):
         "data": "synthetic (seeded normal gradients/weights shaped like the model's projections)",
         "config": {"workload": args.workload, "matrices": n, "elements": elems,
                    "ns_steps": args.ns_steps,
-                   "variant": "gram" if args.variant == 1 else "standard",
+                   "variant": {0: "standard", 1: "gram", 2: "gram-all"}[args.variant],
                    "grad_dtype": str(w.grad_dtype).replace("torch.", ""),
                    "weight_dtype": str(w.weight_dtype).replace("torch.", ""),
                    "momentum_dtype": "float32", "parallelism": f"replicas x{world}",
@@ -584,8 +761,17 @@ def run_gpu(args, rank, world, local_rank):
         "gpu_launches": timed_launches,
         "adamw": adamw,
         "owners": owners,
+        "ns_trace": ns_trace,
         "clocks": clocks,
     }
+    # ---- the benchmark's other configurations (one GPU, default workload only),
+    # each measured on its own after the main workload's buffers are freed
+    if world == 1 and args.workload == DEFAULT_WORKLOAD and not args.no_other_configs:
+        owner = G = M = W = None
+        torch.cuda.empty_cache()
+        gpu_index = int(os.environ.get("GPU_INDEX", "0"))
+        line["other_configs"] = [config_point(dmuon, wl, name, variant, k, dev, gpu_index, peak)
+                                 for name, variant, k in OTHER_CONFIGS]
     if rank == 0 and not args.no_cpu_baseline:
         cms, desc, sec = oracle_sample(args.workload, args.ns_steps)
         line["cpu_baseline"] = {"value": cms, "unit": "ms", "cores": os.cpu_count(),
@@ -605,7 +791,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--ns-steps", type=int, default=5)
-    ap.add_argument("--variant", type=int, default=0, help="0 standard, 1 Gram")
+    ap.add_argument("--variant", type=int, default=0,
+                    help="0 standard, 1 Gram where the library's rule admits it, "
+                         "2 Gram on every matrix with n > m")
     ap.add_argument("--impl", default="dmuon", choices=["dmuon", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-groups", type=int, default=4,
@@ -614,6 +802,13 @@ def main():
     ap.add_argument("--no-launch-count", action="store_true",
                     help="accepted for older command lines; the launch count now comes "
                          "from the library and costs nothing")
+    ap.add_argument("--no-trace", action="store_true",
+                    help="skip the traced step (per-CTA timestamps of the product launches)")
+    ap.add_argument("--trace-out", default="",
+                    help="also save the traced records (numpy .npz) to this file")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the measurements of the other projection-set configurations "
+                         "that follow the default workload's")
     ap.add_argument("--no-adamw", action="store_true",
                     help="skip the AdamW measurement of the non-Muon parameters")
     args = ap.parse_args()

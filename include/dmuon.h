@@ -32,7 +32,9 @@
  *    parameters carry the bytes (no host staging buffer, no pageable copy).
  *  - Calls are asynchronous on `stream`.  Arguments are checked on the host
  *    before anything is enqueued; a bad argument returns an error and
- *    launches nothing.  Device-side failures (a bounded wait that gave up)
+ *    launches nothing.  A call that launches work first clears a pending
+ *    (non-sticky) CUDA error left by earlier work of the calling thread, so
+ *    that DMUON_ERR_CUDA reports only its own failures.  Device-side failures (a bounded wait that gave up)
  *    are recorded in the workspace and reported by dmuon_stream_status.
  *  - Results are deterministic: the same inputs give bit-identical outputs
  *    (no floating-point atomics; fixed reduction orders).
@@ -67,8 +69,19 @@ typedef enum {
 /* Element types of caller tensors. */
 typedef enum { DMUON_F32 = 0, DMUON_BF16 = 1 } dmuon_dtype;
 
-/* Newton-Schulz variant. */
-typedef enum { DMUON_NS_STANDARD = 0, DMUON_NS_GRAM = 1 } dmuon_ns_variant;
+/*
+ * Newton-Schulz variant.
+ *   DMUON_NS_STANDARD  the standard iteration on every matrix.
+ *   DMUON_NS_GRAM      the Gram iteration on each matrix where it saves work
+ *                      (n > m, ns_steps >= 2) AND the library's accuracy rule
+ *                      admits it for that aspect ratio n/m and step count (see
+ *                      dmuon_ns_variant_for); the standard one elsewhere.
+ *   DMUON_NS_GRAM_ALL  the Gram iteration on every matrix with n > m, without
+ *                      the accuracy rule -- for measuring that rule.  Near-square
+ *                      matrices can come out far outside the Newton-Schulz
+ *                      tolerance (bf16 loses the squared small singular values).
+ */
+typedef enum { DMUON_NS_STANDARD = 0, DMUON_NS_GRAM = 1, DMUON_NS_GRAM_ALL = 2 } dmuon_ns_variant;
 
 /* Shape of one parameter: PyTorch (out, in) = (rows, cols). */
 typedef struct { int64_t rows, cols; } dmuon_shape;
@@ -98,6 +111,22 @@ typedef struct { int64_t rows, cols; } dmuon_shape;
  */
 int dmuon_plan(int n, const dmuon_shape* shp, int n_owners, int* owner_of,
                int64_t* offset, int64_t* owner_elems);
+
+/*
+ * dmuon_ns_variant_for -- the form (DMUON_NS_STANDARD or DMUON_NS_GRAM) that a
+ * call with `ns_variant` runs on a (rows, cols) matrix at `ns_steps` steps.
+ * Home page, "VLA and VLM" and the closing credits name Gram Newton-Schulz;
+ * the pages give no rule for when to use it.  This library's rule: Gram only
+ * where it saves work (n > m, ns_steps >= 2) and, for DMUON_NS_GRAM, only
+ * inside a band of aspect ratios n/m, per step count from 2 to 10, in which
+ * the bf16 Gram iteration was measured to stay below 0.9 x the Newton-Schulz
+ * tolerance (2e-2 up to 5 steps, 4e-2 above) on seeded Gaussian inputs of
+ * several sizes; e.g. n/m in [1.75, 7] at 5 steps, [1.5, 8] at 8 steps.  The
+ * calibration assumes well-spread singular values, as Gaussian inputs have.
+ * Returns DMUON_ERR_INVALID_ARG for a bad shape, step count or variant.
+ * Touches no GPU.
+ */
+int dmuon_ns_variant_for(int64_t rows, int64_t cols, int ns_steps, int ns_variant);
 
 /*
  * dmuon_workspace_bytes -- scratch bytes that dmuon_pack / dmuon_ns_batched /
@@ -131,7 +160,7 @@ int dmuon_pack(int n, const dmuon_shape* shp, const void* const* grad, int grad_
  * in place (step 2 above).  packed[offset[i] ...] holds U_i (bf16, (rows, cols)
  * row-major) on entry and O_i (bf16, same layout) on return.
  *   ns_steps       >= 0; 0 returns X0 = U / (||U||_F + eps)
- *   ns_variant     DMUON_NS_STANDARD or DMUON_NS_GRAM
+ *   ns_variant     DMUON_NS_STANDARD, DMUON_NS_GRAM or DMUON_NS_GRAM_ALL
  *   abc            host float[3] (a, b, c), or NULL for (3.4445, -4.7750, 2.0315)
  *   eps            norm epsilon (the standard value is 1e-7)
  *   use_pack_norms 1: take ||U_i|| from the partial sums of the preceding
@@ -162,10 +191,12 @@ int dmuon_unpack_update(int n, const dmuon_shape* shp, void* const* weight,
  * eps = 1e-7, then dmuon_unpack_update, enqueued on `stream`.
  * With the standard variant, ns_steps >= 1 and two or more distinct working
  * shapes (or orientations), the step overlaps its memory-bound kernels with
- * the tensor-core products: it visits the shape groups smallest first, and
- * while one group is orthogonalised the later groups are packed and relaid
- * out and the earlier groups' weights are updated, so that only the first
- * group's pack and the last group's update run alone.  That work runs on a
+ * the tensor-core products: it visits the shape groups in order of size, and
+ * while one group is orthogonalised, later groups are packed and relaid out
+ * and earlier groups' weights are updated, in pieces that each start together
+ * with one long product launch and are sized (by a time model) to finish
+ * inside it; what does not fit -- the packs of the first groups, the last
+ * group's update -- runs alone on `stream`.  The overlapped work runs on a
  * lowest-priority companion stream that the library creates for `stream` on
  * its first call with it (one per caller stream, up to 16 per device; past
  * that, and while `stream` is being captured, a companion shared by the device
@@ -285,6 +316,29 @@ int dmuon_ns_batched_noalloc(int n, const dmuon_shape* shp, void* packed_bf16,
  * counterpart to it.
  */
 int dmuon_noalloc_status(cudaStream_t stream);
+
+/*
+ * Tracing of the Newton-Schulz product launches, for measuring what happens
+ * between and around them (launch gaps, last-wave tails, pipeline fill and
+ * drain).  Between dmuon_trace_begin and dmuon_trace_end, every product launch
+ * made on the device that was current at dmuon_trace_begin writes one record
+ * per CTA into `records` (device memory of that device, 16-byte aligned), in
+ * launch order, until `bytes` is used up; later launches are not traced.
+ * Times are %globaltimer nanoseconds.  In a CTA pair only the first CTA
+ * issues MMAs, so the second CTA's MMA stamps are 0 (also in a CTA that had no
+ * tile).  Tracing costs a few stores per CTA; it changes no result.  Process-
+ * wide: one trace at a time.  dmuon_trace_end returns the number of records
+ * handed out; they are valid once the traced work has completed.
+ */
+typedef struct {
+  uint32_t launch;           /* launch sequence number since dmuon_trace_begin */
+  uint32_t cta;              /* blockIdx.x (CTAs 2k and 2k+1 form pair k) */
+  uint32_t kind;             /* product kind: 0 sym K-major, 1 sym MN-major, 2 full wide, 3 full tall */
+  uint32_t tiles;            /* 256 x 256 tiles of the whole launch */
+  uint64_t t_entry_ns, t_mma_first_ns, t_mma_last_ns, t_exit_ns;
+} dmuon_trace_record;
+int dmuon_trace_begin(void* records, size_t bytes);
+long long dmuon_trace_end(void);
 
 /* Human-readable text for a status code (static storage). */
 const char* dmuon_status_string(int status);

@@ -8,6 +8,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <functional>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -51,6 +52,7 @@ struct Plan {
   int n_std = 0;                    // number of standard buckets
   std::vector<int> bucket_of, idx_in_bucket, internal_of;
   std::vector<long long> chunk_begin, tile_begin;  // per caller matrix
+  std::vector<long long> partial_begin;            // per caller matrix, caller order
   std::vector<int> n_chunks, tiles_r, tiles_c;     // per caller matrix
   std::vector<int> ew_order;                        // table position -> caller matrix
   std::vector<int> ew_pos;                          // caller matrix -> table position
@@ -71,15 +73,44 @@ bool shape_ok(const dmuon_shape& s) {
   return m <= DMUON_MAX_M && n <= DMUON_MAX_N;
 }
 
-bool uses_gram(int variant, int m, int n) {
-  // Reading: the Gram form only for clearly rectangular matrices (n >= 2m),
-  // where it also saves work; square-ish matrices keep the standard form.
-  return variant == DMUON_NS_GRAM && n >= 2 * m;
+// Accuracy rule of the Gram form with bf16 operands.  The Gram iteration
+// works on A = X0 X0^T, whose eigenvalues are the squared singular values of
+// X0: the closer to square a matrix is, the closer to zero its smallest
+// singular values come, and squaring them loses them in bf16 rounding; very
+// wide matrices lose accuracy too, and the rounding compounds with every step.
+// So the form is used only inside a band of aspect ratios n/m that depends on
+// the step count.  Each band is the measured one: over seeded Gaussian inputs
+// with m = 256, 448 (both orientations) and 1024, aspect ratios 1.25 to 8, the
+// worst relative error of the Gram result against the fp64 oracle stayed
+// below 0.9 x the Newton-Schulz tolerance (2e-2 up to 5 steps, 4e-2 above)
+// at every measured ratio from `lo` to `hi`.  Other step counts (0, 1 where
+// Gram saves nothing, 11 and more, not measured) run the standard form.
+struct GramBand {
+  int steps;
+  double lo, hi;  // Gram iff round(lo * m) <= n <= round(hi * m), as the measured shapes
+};
+constexpr GramBand kGramBand[] = {{2, 1.25, 8.0}, {3, 1.25, 8.0}, {4, 1.75, 8.0},
+                                  {5, 1.75, 7.0}, {6, 1.25, 8.0}, {7, 1.5, 8.0},
+                                  {8, 1.5, 8.0},  {9, 1.5, 7.0},  {10, 1.75, 5.83}};
+constexpr int kGramMaxSteps = 10;
+
+bool uses_gram(int variant, int m, int n, int ns_steps) {
+  if (variant == DMUON_NS_GRAM_ALL) return n > m;
+  if (variant != DMUON_NS_GRAM || n <= m) return false;
+  for (const GramBand& b : kGramBand)
+    if (b.steps == ns_steps)
+      return n >= std::llround(b.lo * m) && n <= std::llround(b.hi * m);
+  return false;
 }
 
-int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
+bool variant_ok(int variant) {
+  return variant == DMUON_NS_STANDARD || variant == DMUON_NS_GRAM ||
+         variant == DMUON_NS_GRAM_ALL;
+}
+
+int build_plan(int n, const dmuon_shape* shp, int variant, int ns_steps, Plan& P) {
   if (n < 0 || (n > 0 && shp == nullptr)) return DMUON_ERR_INVALID_ARG;
-  if (variant != DMUON_NS_STANDARD && variant != DMUON_NS_GRAM) return DMUON_ERR_INVALID_ARG;
+  if (!variant_ok(variant)) return DMUON_ERR_INVALID_ARG;
   P = Plan();
   P.n = n;
   P.bucket_of.assign(n, -1);
@@ -87,6 +118,7 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
   P.internal_of.assign(n, -1);
   P.chunk_begin.assign(n, 0);
   P.tile_begin.assign(n, 0);
+  P.partial_begin.assign(n, 0);
   P.n_chunks.assign(n, 0);
   P.tiles_r.assign(n, 0);
   P.tiles_c.assign(n, 0);
@@ -104,7 +136,7 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
     P.tiles_c[i] = int(ceil_div(c, kRelayTile));
     if (r == 0 || c == 0) continue;
     const int m = int(std::min(r, c)), nn = int(std::max(r, c));
-    const Key key(uses_gram(variant, m, nn) ? 1 : 0, m, nn, r > c ? 1 : 0);
+    const Key key(uses_gram(variant, m, nn, ns_steps) ? 1 : 0, m, nn, r > c ? 1 : 0);
     if (!key_to_b.count(key)) {
       key_to_b[key] = -1;
       order.push_back(key);
@@ -130,7 +162,7 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
     const long long r = shp[i].rows, c = shp[i].cols;
     if (r == 0 || c == 0) continue;
     const int m = int(std::min(r, c)), nn = int(std::max(r, c));
-    const int b = key_to_b[Key(uses_gram(variant, m, nn) ? 1 : 0, m, nn, r > c ? 1 : 0)];
+    const int b = key_to_b[Key(uses_gram(variant, m, nn, ns_steps) ? 1 : 0, m, nn, r > c ? 1 : 0)];
     P.bucket_of[i] = b;
     P.idx_in_bucket[i] = int(P.buckets[b].mats.size());
     P.buckets[b].mats.push_back(i);
@@ -169,6 +201,11 @@ int build_plan(int n, const dmuon_shape* shp, int variant, Plan& P) {
     for (int i : B.mats) P.ew_order.push_back(i);
   for (int i = 0; i < n; ++i)
     if (P.bucket_of[i] < 0) P.ew_order.push_back(i);
+  long long partials = 0;
+  for (int i = 0; i < n; ++i) {
+    P.partial_begin[i] = partials;
+    partials += P.n_chunks[i];
+  }
   for (int k = 0; k < n; ++k) {
     const int i = P.ew_order[k];
     P.ew_pos[i] = k;
@@ -431,6 +468,7 @@ int upload_tables(const Request& R, const Plan& P) {
     E.numel = r * c;
     E.active = (r > 0 && c > 0) ? 1 : 0;
     E.chunk_begin = P.chunk_begin[i];
+    E.partial_begin = P.partial_begin[i];
     E.tile_begin = P.tile_begin[i];
     E.n_chunks = P.n_chunks[i];
     E.tiles_r = P.tiles_r[i];
@@ -586,19 +624,23 @@ struct GemmLauncher {
 // Storing B' instead of B keeps B's large diagonal (about b + c once the
 // singular values approach 1) out of the bf16 rounding, where it would be
 // amplified by the cancellation between a X and B X.
-bool ns_standard(const GemmLauncher& L, const Request& R, const Plan& P, unsigned char* ws) {
+// `before(i)`, when given, runs before product launch i = 3*step + {0: X X^T,
+// 1: A A, 2: B X} is enqueued.
+bool ns_standard(const GemmLauncher& L, const Request& R, const Plan& P, unsigned char* ws,
+                 const std::function<bool(int)>& before = nullptr) {
   const float a = R.abc[0], b = R.abc[1], c = R.abc[2];
   float* shift = reinterpret_cast<float*>(ws + P.off_shift);
   const Bucket* bk = reinterpret_cast<const Bucket*>(ws + P.off_bk) + L.b0;
+  auto hook = [&](int i) { return !before || before(i); };
   for (int k = 0; k < R.ns_steps; ++k) {
     const int xin = (k & 1) ? SX1 : SX0, xout = (k & 1) ? SX0 : SX1;
     const bool last = k + 1 == R.ns_steps;
-    if (!L.sym(xin, xin, SM0, SM0, 0.f, 0.f, 1.f)) return false;
+    if (!hook(3 * k) || !L.sym(xin, xin, SM0, SM0, 0.f, 0.f, 1.f)) return false;
     if (launch_diag_shift(bk, L.b1 - L.b0, L.first(), L.n_mats(), SM0, b, c, shift, L.stream) !=
         cudaSuccess)
       return false;
-    if (!L.sym(SM0, SM0, SM0, SM1, 0.f, b, c, shift, -1.f)) return false;
-    if (!L.full(SM1, xin, xin, xout, a, 1.f, last, shift, 1.f)) return false;
+    if (!hook(3 * k + 1) || !L.sym(SM0, SM0, SM0, SM1, 0.f, b, c, shift, -1.f)) return false;
+    if (!hook(3 * k + 2) || !L.full(SM1, xin, xin, xout, a, 1.f, last, shift, 1.f)) return false;
   }
   return true;
 }
@@ -627,6 +669,145 @@ bool ns_gram(const GemmLauncher& L, const Request& R) {
   return L.full(sQ, SX0, SX0, SX0, 0.f, 1.f, true);
 }
 
+// ------------------------------------------------------------------ step pipeline
+// The whole standard step overlaps its memory-bound work (momentum + pack,
+// norm finish and relayout of later buckets; weight update of earlier ones)
+// with the tensor-core products of the current bucket, on a second,
+// low-priority stream.  That work is enqueued in pieces, each one gated to
+// start together with one long product launch and sized to finish inside it:
+// a product launch ready to start while a memory-bound grid still has blocks
+// pending waits until that whole grid is dispatched (an SM filled with
+// memory-bound blocks has no room for a product CTA, about 38k registers, and
+// the block scheduler keeps refilling it from the pending grid), whereas
+// memory-bound blocks enqueued next to a resident product launch run in the
+// room its CTAs leave and never hold up the next launch.  What cannot be
+// placed runs on the caller's stream at full speed: the packs of the first
+// buckets before any product, the last bucket's update after all of them.
+//
+// Time model (only relative times matter): products at kModelTensorFlops
+// (algorithmic), memory-bound work at kModelHbmBytes alone and at
+// kModelCoBytes next to a product launch, of which a piece may plan to use
+// kSlotFill.
+constexpr double kModelTensorFlops = 1.55e15;
+constexpr double kModelHbmBytes = 6.5e12;
+constexpr double kModelCoBytes = 3.0e12;
+constexpr double kSlotFill = 0.45;
+constexpr double kMinPieceBytes = 64.0 * (1 << 20);
+
+enum PieceKind : int { kPiecePack = 0, kPieceFinalize = 1, kPieceRelayout = 2, kPieceUpdate = 3 };
+struct Piece {
+  int kind = 0, bucket = 0;
+  long long lo = 0, hi = 0;  // chunk (pack, update) or tile (relayout) range within the bucket
+};
+
+struct StepSchedule {
+  std::vector<int> ord;                               // bucket order of the products
+  std::vector<char> prepacked;                        // per position: packed on `s` first
+  std::vector<std::vector<std::vector<Piece>>> slot;  // [position][launch]: pieces next to it
+  std::vector<Piece> tail_update;                     // update ranges run on `s` at the end
+  double exposed = 0.0;                               // modelled seconds not hidden
+};
+
+// Modelled seconds of product launch i (= 3*step + phase) of bucket B.
+double model_launch_seconds(const BucketPlan& B, int i) {
+  const double m = B.m, n = B.n, cnt = double(B.mats.size());
+  const int phase = i % 3;
+  const double f = phase == 0 ? m * m * n : phase == 1 ? m * m * m : 2.0 * m * m * n;
+  return cnt * f / kModelTensorFlops;
+}
+
+struct PieceCosts {
+  double pack_chunk, relay_tile, update_chunk;  // bytes moved per chunk / tile
+};
+
+PieceCosts piece_costs(const Request& R) {
+  const double g = R.grad_dt == DMUON_BF16 ? 2.0 : 4.0, w = R.weight_dt == DMUON_BF16 ? 2.0 : 4.0;
+  return {double(kChunk) * (g + 4.0 + 4.0 + 2.0), double(kRelayTile) * kRelayTile * 4.0,
+          double(kChunk) * (2.0 + 2.0 * w)};
+}
+
+// Greedy placement for one bucket order.  Slots are the product launches in
+// issue order; each takes, up to its budget, first the pack/relayout work of
+// the nearest later bucket (needed before that bucket's products start), then
+// the updates of earlier buckets.  A bucket whose pack cannot be finished in
+// the slots before its products is packed on `s` up front instead, and the
+// placement is redone.
+StepSchedule plan_step(const Plan& P, const Request& R, const std::vector<int>& ord) {
+  const int g = int(ord.size());
+  const int launches = 3 * R.ns_steps;
+  const PieceCosts pc = piece_costs(R);
+  StepSchedule S;
+  S.ord = ord;
+  S.prepacked.assign(size_t(g), 0);
+  S.prepacked[0] = 1;
+  for (;;) {
+    S.slot.assign(size_t(g), std::vector<std::vector<Piece>>(size_t(launches)));
+    S.tail_update.clear();
+    // remaining work, as (position, kind, next unit, end unit)
+    struct Todo { int pos, kind; long long lo, hi; };
+    std::vector<Todo> mb, upd;
+    for (int k = 0; k < g; ++k) {
+      const BucketPlan& B = P.buckets[ord[k]];
+      if (!S.prepacked[k]) {
+        mb.push_back({k, kPiecePack, 0, B.chunks});
+        mb.push_back({k, kPieceFinalize, 0, 1});
+        mb.push_back({k, kPieceRelayout, 0, B.tiles});
+      }
+      upd.push_back({k, kPieceUpdate, 0, B.chunks});
+    }
+    size_t mi = 0, ui = 0;
+    int fail = -1;
+    for (int k = 0; k < g && fail < 0; ++k) {
+      // every later bucket's pack must be done before its products start
+      if (mi < mb.size() && mb[mi].pos <= k) fail = mb[mi].pos;
+      for (int i = 0; i < launches && fail < 0; ++i) {
+        double budget = model_launch_seconds(P.buckets[ord[k]], i) * kModelCoBytes * kSlotFill;
+        if (budget < kMinPieceBytes) continue;
+        auto take = [&](Todo& t, double unit_bytes) {
+          const long long can = unit_bytes > 0 ? (long long)(budget / unit_bytes) : t.hi - t.lo;
+          const long long n = std::min(can, t.hi - t.lo);
+          if (n <= 0) return false;
+          S.slot[size_t(k)][size_t(i)].push_back({t.kind, ord[t.pos], t.lo, t.lo + n});
+          budget -= double(n) * unit_bytes;
+          t.lo += n;
+          return t.lo == t.hi;
+        };
+        while (mi < mb.size()) {
+          Todo& t = mb[mi];
+          const double ub = t.kind == kPiecePack ? pc.pack_chunk
+                            : t.kind == kPieceRelayout ? pc.relay_tile : 0.0;
+          if (!take(t, ub)) break;
+          ++mi;
+        }
+        while (ui < upd.size() && upd[ui].pos < k) {
+          if (!take(upd[ui], pc.update_chunk)) break;
+          ++ui;
+        }
+      }
+    }
+    if (fail < 0 && mi < mb.size()) fail = mb[mi].pos;
+    if (fail >= 0) {  // pack that bucket up front and place again
+      S.prepacked[size_t(fail)] = 1;
+      continue;
+    }
+    // updates left over (the unplaced rest of each) run on `s` after the last products
+    for (; ui < upd.size(); ++ui)
+      if (upd[ui].lo < upd[ui].hi)
+        S.tail_update.push_back({kPieceUpdate, ord[upd[ui].pos], upd[ui].lo, upd[ui].hi});
+    break;
+  }
+  S.exposed = 0.0;
+  for (int k = 0; k < g; ++k) {
+    const BucketPlan& B = P.buckets[ord[k]];
+    if (S.prepacked[size_t(k)])
+      S.exposed += (double(B.chunks) * pc.pack_chunk + double(B.tiles) * pc.relay_tile) /
+                   kModelHbmBytes;
+  }
+  for (const Piece& t : S.tail_update)
+    S.exposed += double(t.hi - t.lo) * pc.update_chunk / kModelHbmBytes;
+  return S;
+}
+
 // Events used to order the two streams of an overlapped step; released when
 // the call returns (the driver keeps a pending event alive until it fires).
 struct EventSet {
@@ -647,8 +828,11 @@ struct EventSet {
 
 int run(const Request& R) {
   if (R.n < 0 || (R.n > 0 && R.shp == nullptr)) return DMUON_ERR_INVALID_ARG;
+  // a pending, non-sticky error of earlier work on this thread is not ours:
+  // clear it, so that the launch checks below report only this call's failures
+  (void)cudaGetLastError();
   Plan P;
-  int st = build_plan(R.n, R.shp, R.variant, P);
+  int st = build_plan(R.n, R.shp, R.variant, R.ns_steps, P);
   if (st != DMUON_OK) return st;
   st = check_request(R, P);
   if (st != DMUON_OK) return st;
@@ -682,15 +866,11 @@ int run(const Request& R) {
     return r;
   };
 
-  // A whole standard step over two or more buckets runs as a pipeline over the
-  // buckets, smallest first, with the memory-bound kernels on a second,
-  // low-priority stream: while one bucket's products run, the later buckets
-  // are packed and relaid out and the earlier buckets' weights are updated.
-  // Only the first bucket's pack and the last bucket's update are exposed.
-  //   stream s : mb(0) | NS(0) | NS(1) | ... | NS(G-1), update(G-1) | join
-  //   aux      :       | mb(1), mb(2), ..., mb(G-1), update(0), ..., update(G-2)
-  // (mb = momentum + pack, norm finish, relayout; NS(k) waits for mb(k),
-  // update(k) for NS(k))
+  // A whole standard step over two or more buckets overlaps its memory-bound
+  // work with the products (see plan_step).  Candidate bucket orders: smallest
+  // first (short first products, small up-front packs), and the same with the
+  // smallest of the later buckets moved last (the last bucket's update is
+  // exposed); the one with less modelled exposed time runs.
   const bool overlap = R.do_pack && R.do_ns && R.do_update && R.ns_steps > 0 && P.n_std >= 2 &&
                        P.n_std == nb && D.aux != nullptr;
   if (overlap) {
@@ -699,34 +879,90 @@ int run(const Request& R) {
     std::stable_sort(ord.begin(), ord.end(), [&](int a, int b) {
       return P.buckets[a].chunks < P.buckets[b].chunks;
     });
-    EventSet ev;  // [0, nb): mb(k) done; [nb, 2nb): NS(k) done; 2nb: aux done
-    if (!ev.create(2 * nb + 1)) return DMUON_ERR_CUDA;
+    StepSchedule S = plan_step(P, R, ord);
+    if (nb >= 3) {
+      std::vector<int> alt = ord;
+      const int b = alt[1];
+      alt.erase(alt.begin() + 1);
+      alt.push_back(b);
+      StepSchedule T = plan_step(P, R, alt);
+      if (T.exposed < S.exposed) S = std::move(T);
+    }
     cudaStream_t x = aux_stream_for(D, s);
-    auto mb = [&](int k, cudaStream_t st) {
-      const EwRange r = range_of(ord[k], ord[k] + 1);
-      return launch_momentum_pack(r, gbf16, R.beta, packed, partials, st) == cudaSuccess &&
-             launch_norm_finalize(r, partials, R.eps, inv, st) == cudaSuccess &&
-             launch_relayout(r, packed, inv, st) == cudaSuccess &&
-             cudaEventRecord(ev.e[k], st) == cudaSuccess;
-    };
-    if (!mb(0, s)) return DMUON_ERR_CUDA;
-    if (cudaStreamWaitEvent(x, ev.e[0], 0) != cudaSuccess) return DMUON_ERR_CUDA;
-    for (int k = 1; k < nb; ++k)
-      if (!mb(k, x)) return DMUON_ERR_CUDA;
+    size_t n_slots = 0;
+    for (const auto& v : S.slot)
+      for (const auto& w : v) n_slots += w.empty() ? 0 : 1;
+    EventSet ev;  // [0, nb): position k's pack done on aux; nb: aux done; then one per used slot
+    if (!ev.create(nb + 1 + int(n_slots))) return DMUON_ERR_CUDA;
+    size_t next_ev = size_t(nb) + 1;
+    auto bucket_range = [&](int b) { return range_of(b, b + 1); };
+    // packs up front, on `s`, at full speed
     for (int k = 0; k < nb; ++k) {
-      if (k > 0 && cudaStreamWaitEvent(s, ev.e[k], 0) != cudaSuccess) return DMUON_ERR_CUDA;
-      if (!ns_standard(GemmLauncher(P, R, D.max_clusters, ws, ord[k], ord[k] + 1, s), R, P, ws) ||
-          cudaEventRecord(ev.e[nb + k], s) != cudaSuccess)
+      if (!S.prepacked[size_t(k)]) continue;
+      const EwRange r = bucket_range(S.ord[size_t(k)]);
+      if (launch_momentum_pack(r, gbf16, R.beta, packed, partials, s) != cudaSuccess ||
+          launch_norm_finalize(r, partials, R.eps, inv, s) != cudaSuccess ||
+          launch_relayout(r, packed, inv, s) != cudaSuccess)
         return DMUON_ERR_CUDA;
     }
-    for (int k = 0; k + 1 < nb; ++k)
-      if (cudaStreamWaitEvent(x, ev.e[nb + k], 0) != cudaSuccess ||
-          launch_update(range_of(ord[k], ord[k] + 1), wbf16, R.lr, packed, x) != cudaSuccess)
+    std::vector<int> pos_of(static_cast<size_t>(nb), 0);
+    for (int k = 0; k < nb; ++k) pos_of[size_t(S.ord[size_t(k)])] = k;
+    // one piece on the aux stream
+    auto run_piece = [&](const Piece& pc) {
+      EwRange r = bucket_range(pc.bucket);
+      switch (pc.kind) {
+        case kPiecePack:
+          r.chunk_base += pc.lo;
+          r.chunks = pc.hi - pc.lo;
+          return launch_momentum_pack(r, gbf16, R.beta, packed, partials, x) == cudaSuccess;
+        case kPieceFinalize:
+          return launch_norm_finalize(r, partials, R.eps, inv, x) == cudaSuccess;
+        case kPieceRelayout: {
+          r.tile_base += pc.lo;
+          r.tiles = pc.hi - pc.lo;
+          if (launch_relayout(r, packed, inv, x) != cudaSuccess) return false;
+          // the bucket is ready for its products after its last relayout piece
+          if (pc.hi == P.buckets[pc.bucket].tiles &&
+              cudaEventRecord(ev.e[size_t(pos_of[size_t(pc.bucket)])], x) != cudaSuccess)
+            return false;
+          return true;
+        }
+        default:
+          r.chunk_base += pc.lo;
+          r.chunks = pc.hi - pc.lo;
+          return launch_update(r, wbf16, R.lr, packed, x) == cudaSuccess;
+      }
+    };
+    for (int k = 0; k < nb; ++k) {
+      if (!S.prepacked[size_t(k)] && cudaStreamWaitEvent(s, ev.e[size_t(k)], 0) != cudaSuccess)
         return DMUON_ERR_CUDA;
-    if (cudaEventRecord(ev.e[2 * nb], x) != cudaSuccess ||
-        launch_update(range_of(ord[nb - 1], ord[nb - 1] + 1), wbf16, R.lr, packed, s) !=
-            cudaSuccess ||
-        cudaStreamWaitEvent(s, ev.e[2 * nb], 0) != cudaSuccess)
+      const auto& slots = S.slot[size_t(k)];
+      auto before = [&](int i) {
+        const auto& pieces = slots[size_t(i)];
+        if (pieces.empty()) return true;
+        // the pieces start together with this product launch
+        cudaEvent_t e = ev.e[next_ev++];
+        if (cudaEventRecord(e, s) != cudaSuccess || cudaStreamWaitEvent(x, e, 0) != cudaSuccess)
+          return false;
+        for (const Piece& pc : pieces)
+          if (!run_piece(pc)) return false;
+        return true;
+      };
+      if (!ns_standard(GemmLauncher(P, R, D.max_clusters, ws, S.ord[size_t(k)],
+                                    S.ord[size_t(k)] + 1, s),
+                       R, P, ws, before))
+        return DMUON_ERR_CUDA;
+    }
+    for (const Piece& t : S.tail_update) {
+      EwRange r = bucket_range(t.bucket);
+      r.chunk_base += t.lo;
+      r.chunks = t.hi - t.lo;
+      if (launch_update(r, wbf16, R.lr, packed, s) != cudaSuccess) return DMUON_ERR_CUDA;
+    }
+    // join: only if anything ran on the aux stream (under stream capture, an
+    // aux stream that never forked from `s` is not part of the capture)
+    if (n_slots > 0 && (cudaEventRecord(ev.e[size_t(nb)], x) != cudaSuccess ||
+                        cudaStreamWaitEvent(s, ev.e[size_t(nb)], 0) != cudaSuccess))
       return DMUON_ERR_CUDA;
     return DMUON_OK;
   }
@@ -806,7 +1042,7 @@ int dmuon_ns_batched_noalloc(int n, const dmuon_shape* shp, void* packed_bf16,
   // host-side checks first: nothing is enqueued for a rejected call
   if (n < 0 || (n > 0 && shp == nullptr)) return DMUON_ERR_INVALID_ARG;
   Plan P;
-  int st = build_plan(n, shp, ns_variant, P);
+  int st = build_plan(n, shp, ns_variant, ns_steps, P);
   if (st != DMUON_OK) return st;
   if (P.total > size_t(DMUON_NOALLOC_SCRATCH_BYTES)) return DMUON_ERR_WORKSPACE;
   if (n == 0) return DMUON_OK;
@@ -871,9 +1107,25 @@ int dmuon_plan(int n, const dmuon_shape* shp, int n_owners, int* owner_of, int64
 }
 
 size_t dmuon_workspace_bytes(int n, const dmuon_shape* shp, int ns_variant) {
-  Plan P;
-  if (build_plan(n, shp, ns_variant, P) != DMUON_OK) return 0;
-  return P.total;
+  // Which matrices run the Gram form depends on ns_steps: size for every step
+  // count the rule distinguishes (1 and kGramMaxSteps + 1 stand for all others).
+  size_t most = 0;
+  const int last = ns_variant == DMUON_NS_GRAM ? kGramMaxSteps + 1 : 1;
+  for (int k = 1; k <= last; ++k) {
+    Plan P;
+    if (build_plan(n, shp, ns_variant, k, P) != DMUON_OK) return 0;
+    most = std::max(most, P.total);
+  }
+  return most;
+}
+
+int dmuon_ns_variant_for(int64_t rows, int64_t cols, int ns_steps, int ns_variant) {
+  const dmuon_shape s{rows, cols};
+  if (!shape_ok(s) || ns_steps < 0 || ns_steps > kMaxNsSteps || !variant_ok(ns_variant))
+    return DMUON_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return DMUON_NS_STANDARD;
+  const int m = int(std::min(rows, cols)), nn = int(std::max(rows, cols));
+  return uses_gram(ns_variant, m, nn, ns_steps) ? DMUON_NS_GRAM : DMUON_NS_STANDARD;
 }
 
 int dmuon_pack(int n, const dmuon_shape* shp, const void* const* grad, int grad_dt,
@@ -1029,6 +1281,19 @@ int dmuon_debug_wait_timeout(void* workspace, size_t ws_bytes, int budget_us,
     return DMUON_ERR_CUDA;
   return DMUON_OK;
 }
+
+static_assert(sizeof(dmuon_trace_record) == sizeof(TraceRec), "trace record layout");
+
+int dmuon_trace_begin(void* records, size_t bytes) {
+  if (records == nullptr || bytes < sizeof(TraceRec)) return DMUON_ERR_INVALID_ARG;
+  if (!aligned(records, 16)) return DMUON_ERR_ALIGNMENT;
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return DMUON_ERR_CUDA;
+  trace_begin(records, bytes / sizeof(TraceRec), d);
+  return DMUON_OK;
+}
+
+long long dmuon_trace_end(void) { return trace_end(); }
 
 const char* dmuon_status_string(int status) {
   switch (status) {

@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kEwThreads) momentum_pack_kernel(const EwMat* 
     }
   }
   const float tot = block_sum(ss);
-  if (threadIdx.x == 0) partials[chunk] = tot;
+  if (threadIdx.x == 0) partials[E.partial_begin + (chunk - E.chunk_begin)] = tot;
 }
 
 __global__ void __launch_bounds__(kEwThreads) norm_partials_kernel(const EwMat* __restrict__ ew,
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kEwThreads) norm_partials_kernel(const EwMat* 
     }
   }
   const float tot = block_sum(ss);
-  if (threadIdx.x == 0) partials[chunk] = tot;
+  if (threadIdx.x == 0) partials[E.partial_begin + (chunk - E.chunk_begin)] = tot;
 }
 
 __global__ void __launch_bounds__(kEwThreads) norm_finalize_kernel(const EwMat* __restrict__ ew,
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kEwThreads) norm_finalize_kernel(const EwMat* 
   const EwMat& E = ew[blockIdx.x];
   double s = 0.0;
   for (int c = threadIdx.x; c < E.n_chunks; c += kEwThreads)
-    s += (double)partials[E.chunk_begin + c];
+    s += (double)partials[E.partial_begin + c];
   red[threadIdx.x] = s;
   __syncthreads();
   for (int w = kEwThreads / 2; w > 0; w >>= 1) {

@@ -21,6 +21,10 @@ size_t ns_gemm_smem_bytes();
 // (clusters of two) can be resident at once.
 cudaError_t ns_gemm_prepare(int num_sms, int* max_clusters);
 cudaError_t launch_ns_gemm(const GemmArgs& g, int kind, int max_clusters, cudaStream_t s);
+// Product-launch tracing: while active, every product launch on `device` that
+// still fits writes one TraceRec per CTA into `buf` (room for `records`).
+void trace_begin(void* buf, size_t records, int device);
+long long trace_end();  // stops tracing; returns the records handed out
 // Per-matrix diagonal shift b*s + c*s^2 with s = trace(A)/m, A = slot `slot`.
 cudaError_t launch_diag_shift(const Bucket* buckets, int n_buckets, int first_internal,
                               int n_mats, int slot, float b, float c, float* shift,

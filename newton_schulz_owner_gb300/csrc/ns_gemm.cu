@@ -42,6 +42,8 @@
 
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 namespace dm {
 namespace {
 
@@ -61,7 +63,8 @@ constexpr int kBarBytes = 512;
 constexpr size_t kSmemBytes =
     size_t(kStages) * kStageBytes + kEpiBytes + 1024 + kBarBytes;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory above the sm_100 per-block limit");
-static_assert((2 * kStages + 5 + 2 * kEpiWarps) * 8 + 8 <= kBarBytes, "barrier area too small");
+static_assert((2 * kStages + 5 + 2 * kEpiWarps) * 8 + 8 + 16 <= kBarBytes,
+              "barrier area too small");
 // After a bounded wait gives up, wait this long before leaving so that copies
 // and MMAs already issued to this CTA's shared memory / TMEM have landed.
 constexpr long long kAbortSettleCycles = 400000;
@@ -163,6 +166,17 @@ DM_DEV void producer(const GemmArgs& g, uint32_t rank, uint8_t* sA, uint8_t* sB,
     const int KB = (k_extent<KIND>(g, B) + kBK - 1) / kBK;
     const int row0 = T.ti * kTileM + int(rank) * kCtaM;        // this CTA's rows of L
     const int col0 = T.tj * kTileN + int(rank) * (kTileN / 2);  // this CTA's columns of R
+    // Symmetric products stream K = n (X X^T) through every tile; when a
+    // matrix's triangle takes more than one wave of tiles, each wave reads all
+    // of X again.  Every other wave walks K backwards, so it starts on the K
+    // blocks the previous wave read last, which are still in L2.  The wave is
+    // counted within the tile's bucket, so a tile accumulates in the same
+    // order whether its bucket is launched alone or with others (and matches
+    // the real waves exactly when it is launched alone).  The MMA side does
+    // not care about the order: it accumulates whatever the stages hold and
+    // zeroes on the first block it sees.
+    const bool k_reverse =
+        !Kind<KIND>::full && (((g.tile_base + t - B.sym_begin) / clusters) & 1) != 0;
     for (int kb = 0; kb < KB; ++kb) {
       if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
         raise_abort(g.err, abort_flag);
@@ -172,7 +186,7 @@ DM_DEV void producer(const GemmArgs& g, uint32_t rank, uint8_t* sA, uint8_t* sB,
       uint8_t* a = sA + stage * kAStage;
       uint8_t* b = sB + stage * kBStage;
       const uint32_t bar = leader_full + uint32_t(stage) * 8u;
-      const int k0 = kb * kBK;
+      const int k0 = (k_reverse ? KB - 1 - kb : kb) * kBK;
       if (Kind<KIND>::l_mn) {  // 64 K-rows x 64 rows of L per box
         tma_load_3d_pair(a, mapL, bar, row0, k0, T.mat);
         tma_load_3d_pair(a + kBox, mapL, bar, row0 + 64, k0, T.mat);
@@ -198,7 +212,8 @@ DM_DEV void producer(const GemmArgs& g, uint32_t rank, uint8_t* sA, uint8_t* sB,
 template <int KIND>
 DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* full_bar,
                        uint64_t* empty_bar, uint64_t* tfull, uint64_t* tempty,
-                       uint64_t* drain_bar, uint32_t tmem_base, volatile int* abort_flag) {
+                       uint64_t* drain_bar, uint32_t tmem_base, volatile int* abort_flag,
+                       unsigned long long* tstamp) {
   constexpr uint32_t idesc = idesc_bf16(kTileM, kTileN, Kind<KIND>::l_mn, Kind<KIND>::r_mn);
   const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
   const int clusters = int(cluster_count_x());
@@ -235,6 +250,7 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
         break;
       }
       tc_fence_after();
+      if (g.trace != nullptr && tstamp[0] == 0) tstamp[0] = globaltimer_ns();
       const uint64_t ad = a_desc + uint64_t(stage * (kAStage >> 4));
       const uint64_t bd = b_desc + uint64_t(stage * (kBStage >> 4));
 #pragma unroll
@@ -252,6 +268,7 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
   // Every issued MMA must finish before TMEM and shared memory go away.
   umma_commit_pair(drain_bar, 0x1);
   (void)mbar_wait(drain_bar, 0, nullptr);
+  if (g.trace != nullptr && tstamp[0] != 0) tstamp[1] = globaltimer_ns();
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -542,6 +559,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   uint64_t* aux_bar = drain_bar + 1;     // two per epilogue warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + 2 * kEpiWarps);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // first / last MMA time of this CTA (traced launches only)
+  unsigned long long* tstamp = reinterpret_cast<unsigned long long*>(aux_bar + 2 * kEpiWarps + 1);
+  const unsigned long long t_entry = g.trace != nullptr ? globaltimer_ns() : 0ull;
 
   const int warp = threadIdx.x >> 5;
   const uint32_t rank = cluster_rank();
@@ -557,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     mbar_init(drain_bar, 1);
     for (int a = 0; a < 2 * kEpiWarps; ++a) mbar_init(&aux_bar[a], 1);  // lane 0's expect_tx
     *abort_flag = 0;
+    tstamp[0] = tstamp[1] = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -573,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   } else if (threadIdx.x == 32) {
     if (rank == 0)
       mma_issuer<KIND>(g, sA, sB, full_bar, empty_bar, tfull, tempty, drain_bar, tmem_base,
-                       abort_flag);
+                       abort_flag, tstamp);
   } else if (warp >= 2) {
     epilogue<KIND>(g, rank, tfull, tempty, aux_bar, smem_u32(sE), tmem_base, abort_flag);
   }
@@ -589,6 +610,18 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+  if (g.trace != nullptr && threadIdx.x == 0) {
+    TraceRec r;
+    r.launch = g.trace_launch;
+    r.cta = blockIdx.x;
+    r.kind = uint32_t(KIND);
+    r.tiles = uint32_t(g.total_tiles);
+    r.t_entry = t_entry;
+    r.t_mma_first = tstamp[0];
+    r.t_mma_last = tstamp[1];
+    r.t_exit = globaltimer_ns();
+    g.trace[blockIdx.x] = r;
   }
 }
 
@@ -679,9 +712,47 @@ cudaError_t ns_gemm_prepare(int num_sms, int* max_clusters) {
   return cudaSuccess;
 }
 
-cudaError_t launch_ns_gemm(const GemmArgs& g, int kind, int max_clusters, cudaStream_t s) {
-  if (g.total_tiles <= 0 || g.n_buckets <= 0) return cudaSuccess;
-  const int clusters = g.total_tiles < max_clusters ? g.total_tiles : max_clusters;
+namespace {
+// Trace of product launches (process-wide; see dmuon_trace_begin).
+std::mutex g_trace_mu;
+TraceRec* g_trace_buf = nullptr;
+size_t g_trace_cap = 0, g_trace_used = 0;
+uint32_t g_trace_launches = 0;
+int g_trace_device = -1;
+}  // namespace
+
+void trace_begin(void* buf, size_t records, int device) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_device = device;
+  g_trace_buf = static_cast<TraceRec*>(buf);
+  g_trace_cap = records;
+  g_trace_used = 0;
+  g_trace_launches = 0;
+}
+
+long long trace_end() {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  const long long n = (long long)g_trace_used;
+  g_trace_buf = nullptr;
+  g_trace_cap = g_trace_used = 0;
+  return n;
+}
+
+cudaError_t launch_ns_gemm(const GemmArgs& g_in, int kind, int max_clusters, cudaStream_t s) {
+  if (g_in.total_tiles <= 0 || g_in.n_buckets <= 0) return cudaSuccess;
+  const int clusters = g_in.total_tiles < max_clusters ? g_in.total_tiles : max_clusters;
+  GemmArgs g = g_in;
+  g.trace = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    int dev = -1;
+    if (g_trace_buf != nullptr && g_trace_used + size_t(2 * clusters) <= g_trace_cap &&
+        cudaGetDevice(&dev) == cudaSuccess && dev == g_trace_device) {
+      g.trace = g_trace_buf + g_trace_used;
+      g.trace_launch = g_trace_launches++;
+      g_trace_used += size_t(2 * clusters);
+    }
+  }
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg = pair_config(clusters, s, &attr);
   switch (kind) {

@@ -210,6 +210,12 @@ DM_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "
 // (rank 0) issues it, each CTA holds half of A (M rows) and half of B (N) in
 // its own shared memory at the same offsets, and each CTA's TMEM receives its
 // 128 rows of the accumulator.
+DM_DEV unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 DM_DEV uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

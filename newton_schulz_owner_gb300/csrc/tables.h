@@ -37,6 +37,10 @@ struct EwMat {
   long long packed_off;    // element offset of the packed segment
   long long numel;         // rows * cols
   long long chunk_begin;   // first elementwise chunk
+  long long partial_begin; // first norm partial sum: caller order, so that the
+                           // partials' layout does not depend on the variant
+                           // (a pack and a later Newton-Schulz call may plan
+                           // their buckets differently)
   long long tile_begin;    // first relayout tile
   int rows, cols;
   int n_chunks;
@@ -106,6 +110,18 @@ enum ProductKind : int { kSymK = 0, kSymMN = 1, kFullWide = 2, kFullTall = 3 };
 // tile; each CTA holds 128 of its rows (and loads half of its columns' operand).
 constexpr int kTileM = 256, kTileN = 256, kCtaM = 128, kBK = 64;
 
+// One record per CTA of a traced product launch (see dmuon_trace_begin):
+// %globaltimer nanoseconds at kernel entry, at the leader's first MMA issue,
+// after the leader's last MMA completed, and at exit (MMA stamps are 0 in the
+// second CTA of a pair and in a CTA that had no tile).
+struct TraceRec {
+  uint32_t launch;               // sequence number of the launch since tracing began
+  uint32_t cta;                  // blockIdx.x
+  uint32_t kind;                 // ProductKind
+  uint32_t tiles;                // tiles of the whole launch
+  unsigned long long t_entry, t_mma_first, t_mma_last, t_exit;
+};
+
 // Launch arguments of the grouped Newton-Schulz product kernel.
 //   symmetric product (m x m output, upper-triangle tiles, mirrored):
 //     out = alpha * I + beta * aux + gamma * (L R^T)
@@ -131,6 +147,8 @@ struct GemmArgs {
   int final_out;                 // full product: write O into `packed`
   float alpha, beta, gamma;
   float shift_sign;
+  TraceRec* trace;               // this launch's records (gridDim.x of them), or null
+  uint32_t trace_launch;
 };
 
 }  // namespace dm

@@ -22,16 +22,16 @@ _lib = ctypes.CDLL(_LIB_PATH)
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = \
     0, -1, -2, -3, -4, -5, -6
 F32, BF16 = 0, 1
-NS_STANDARD, NS_GRAM = 0, 1
+NS_STANDARD, NS_GRAM, NS_GRAM_ALL = 0, 1, 2
 PACK_ALIGN_ELEMS = 128
 DEFAULT_ABC = (3.4445, -4.7750, 2.0315)
 
-EXPORTED = ("dmuon_plan", "dmuon_workspace_bytes", "dmuon_pack", "dmuon_ns_batched",
+EXPORTED = ("dmuon_plan", "dmuon_workspace_bytes", "dmuon_ns_variant_for", "dmuon_pack", "dmuon_ns_batched",
             "dmuon_unpack_update", "dmuon_muon_step", "dmuon_stream_status",
             "dmuon_debug_wait_timeout", "dmuon_ns_batched_noalloc", "dmuon_noalloc_status",
             "dmuon_adamw",
             "dmuon_adamw_workspace_bytes", "dmuon_status_string", "dmuon_version",
-            "dmuon_launch_count")
+            "dmuon_launch_count", "dmuon_trace_begin", "dmuon_trace_end")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -48,6 +48,8 @@ _lib.dmuon_plan.argtypes = [_i, _ShapeP, _i, ctypes.POINTER(ctypes.c_int), _i64p
 _lib.dmuon_plan.restype = _i
 _lib.dmuon_workspace_bytes.argtypes = [_i, _ShapeP, _i]
 _lib.dmuon_workspace_bytes.restype = _sz
+_lib.dmuon_ns_variant_for.argtypes = [ctypes.c_int64, ctypes.c_int64, _i, _i]
+_lib.dmuon_ns_variant_for.restype = _i
 _lib.dmuon_pack.argtypes = [_i, _ShapeP, _VPP, _i, _VPP, _f, _vp, _i64p, _vp, _sz, _vp]
 _lib.dmuon_pack.restype = _i
 _lib.dmuon_ns_batched.argtypes = [_i, _ShapeP, _vp, _i64p, _i, _i, ctypes.POINTER(ctypes.c_float),
@@ -79,6 +81,11 @@ _lib.dmuon_version.argtypes = []
 _lib.dmuon_version.restype = _i
 _lib.dmuon_launch_count.argtypes = [_i]
 _lib.dmuon_launch_count.restype = ctypes.c_longlong
+_lib.dmuon_trace_begin.argtypes = [_vp, _sz]
+_lib.dmuon_trace_begin.restype = _i
+_lib.dmuon_trace_end.argtypes = []
+_lib.dmuon_trace_end.restype = ctypes.c_longlong
+TRACE_RECORD_BYTES = 48
 
 
 class DMuonError(RuntimeError):
@@ -169,6 +176,15 @@ def workspace_bytes(shapes: Sequence[Tuple[int, int]], variant: int = NS_STANDAR
     return int(_lib.dmuon_workspace_bytes(len(shapes), _shapes(shapes), int(variant)))
 
 
+def ns_variant_for(shape: Tuple[int, int], ns_steps: int, variant: int = NS_GRAM) -> int:
+    """The Newton-Schulz form (NS_STANDARD or NS_GRAM) a call with `variant`
+    runs on one matrix of this shape at `ns_steps` steps (host only)."""
+    st = int(_lib.dmuon_ns_variant_for(int(shape[0]), int(shape[1]), int(ns_steps), int(variant)))
+    if st < 0:
+        raise DMuonError(st, "dmuon_ns_variant_for")
+    return st
+
+
 def pack(shapes, grads, momenta, beta, packed, offsets, workspace, stream=None) -> None:
     n = len(shapes)
     gdt = _dtype(grads[0]) if n else BF16
@@ -256,6 +272,24 @@ def debug_wait_timeout(workspace, budget_us: int, stream=None) -> None:
     nbytes = 0 if workspace is None else workspace.numel()
     _check(_lib.dmuon_debug_wait_timeout(ws, nbytes, int(budget_us), _stream(stream)),
            "dmuon_debug_wait_timeout")
+
+
+def trace_begin(buffer) -> None:
+    """Record one timestamp record per CTA of every product launch into
+    `buffer` (a uint8 CUDA tensor) until :func:`trace_end`."""
+    _check(_lib.dmuon_trace_begin(_addr(buffer), buffer.numel()), "dmuon_trace_begin")
+
+
+def trace_end(buffer):
+    """Stop tracing; return the records as a dict of int64 CPU tensors (read
+    after the traced work has completed)."""
+    n = int(_lib.dmuon_trace_end())
+    raw = buffer[:n * TRACE_RECORD_BYTES].cpu()
+    u32 = raw.view(torch.int32).view(n, 12).to(torch.int64) & 0xFFFFFFFF
+    u64 = raw.view(torch.int64).view(n, 6)
+    return {"launch": u32[:, 0], "cta": u32[:, 1], "kind": u32[:, 2], "tiles": u32[:, 3],
+            "t_entry": u64[:, 2], "t_mma_first": u64[:, 3], "t_mma_last": u64[:, 4],
+            "t_exit": u64[:, 5]}
 
 
 class MuonOwner:

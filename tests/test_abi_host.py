@@ -138,3 +138,40 @@ def test_binding_fails_loudly_without_library(tmp_path):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError):
         spec.loader.exec_module(mod)
+
+
+def test_ns_variant_rule_properties(dm):
+    """The Gram rule (host only): standard unless Gram saves work (n > m and at
+    least 2 steps) and the step count is one the rule was measured for (2..10);
+    never for square matrices; the same for a matrix and its transpose; for a
+    fixed step count the Gram aspect ratios form one interval (a band); the
+    band edges sit where the measurement put them; GRAM_ALL takes every n > m,
+    STANDARD none."""
+    ratios = [1.0 + 0.05 * i for i in range(1, 200)]           # 1.05 .. 10.95
+    for k in range(0, 14):
+        for m in (64, 333, 1024):
+            assert dm.ns_variant_for((m, m), k, dm.NS_GRAM) == dm.NS_STANDARD
+            picks = []
+            for r in ratios:
+                n = int(round(r * m))
+                got = dm.ns_variant_for((m, n), k, dm.NS_GRAM)
+                assert got == dm.ns_variant_for((n, m), k, dm.NS_GRAM)
+                if k < 2 or k > 10:
+                    assert got == dm.NS_STANDARD
+                picks.append(got)
+                assert dm.ns_variant_for((m, n), k, dm.NS_GRAM_ALL) == dm.NS_GRAM
+                assert dm.ns_variant_for((m, n), k, dm.NS_STANDARD) == dm.NS_STANDARD
+            on = [i for i, p in enumerate(picks) if p == dm.NS_GRAM]
+            if on:   # one contiguous band
+                assert on == list(range(on[0], on[-1] + 1)), (m, k)
+    m = 1024
+    edge = {5: [(1.5, 0), (1.75, 1), (7.0, 1), (7.5, 0)], 8: [(1.25, 0), (1.5, 1), (8.0, 1), (8.5, 0)],
+            10: [(1.5, 0), (1.75, 1), (5.83, 1), (6.5, 0)], 3: [(1.25, 1), (8.0, 1), (9.0, 0)]}
+    for k, pts in edge.items():
+        for r, want in pts:
+            got = dm.ns_variant_for((m, int(round(r * m))), k, dm.NS_GRAM)
+            assert got == (dm.NS_GRAM if want else dm.NS_STANDARD), (k, r)
+    with pytest.raises(dm.DMuonError):
+        dm.ns_variant_for((4, 8), -1, dm.NS_GRAM)
+    with pytest.raises(dm.DMuonError):
+        dm.ns_variant_for((4, 8), 5, 7)

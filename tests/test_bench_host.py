@@ -60,3 +60,40 @@ def test_layer_traffic_record_is_above_the_algorithmic_bytes():
     assert stored["dram_bytes_per_ns_phase"] == pytest.approx(
         stored["dram_bytes_per_layer_iteration"] * 32 * 5)
     assert callable(b.blas_name) and isinstance(b.blas_name(), str) and b.blas_name()
+
+
+def test_trace_summary_splits_pair_time():
+    """Two launches of two pairs each (four CTAs), hand-made timestamps in ns:
+    launch 0 runs 0..1000 (pair 0 MMA 100..900, pair 1 MMA 100..500, exits at
+    600), launch 1 starts after a 200 ns gap and runs 1200..2000 (both pairs
+    MMA 1300..1900).  Window 2000 ns x 2 pairs = 4000 pair-ns; MMA-active
+    800 + 400 + 600 + 600 = 2400; resident 1000 + 600 + 800 + 800 = 3200."""
+    import torch
+    b = _bench()
+    T = lambda v: torch.tensor(v, dtype=torch.int64)
+    rec = {"launch": T([0, 0, 0, 0, 1, 1, 1, 1]), "cta": T([0, 1, 2, 3, 0, 1, 2, 3]),
+           "kind": T([0] * 8), "tiles": T([2] * 8),
+           "t_entry": T([0, 0, 0, 0, 1200, 1200, 1200, 1200]),
+           "t_mma_first": T([100, 0, 100, 0, 1300, 0, 1300, 0]),
+           "t_mma_last": T([900, 0, 500, 0, 1900, 0, 1900, 0]),
+           "t_exit": T([1000, 1000, 600, 600, 2000, 2000, 2000, 2000])}
+    s = b.trace_summary(rec, step_ms=0.003)
+    assert s["launches"] == 2 and s["pairs"] == 2
+    assert s["product_window_ms"] == pytest.approx(2000e-6)
+    assert s["mma_active_frac"] == pytest.approx(2400 / 4000)
+    assert s["fill_drain_frac"] == pytest.approx(800 / 4000)
+    assert s["not_resident_frac"] == pytest.approx(800 / 4000)
+    assert s["launch_gaps_ms"] == pytest.approx(200e-6)
+    assert s["recoverable_ms_upper_bound"] == pytest.approx(1600e-6 / 2)
+
+
+@pytest.mark.parametrize("steps", [0, 1, 2, 3, 5, 8])
+def test_bench_flop_counts_agree_with_the_oracle(steps):
+    """The bench counts algorithmic flops itself (its GPU leg does not touch
+    the oracle); both counts must agree with the oracle's."""
+    import oracle
+    b = _bench()
+    shapes = [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336), (300, 7), (1, 1)]
+    assert b.ns_flops(shapes, steps) == pytest.approx(oracle.ns_flops_algorithmic(shapes, steps))
+    assert b.gram_flops(shapes, steps) == pytest.approx(
+        oracle.gram_ns_flops_algorithmic(shapes, steps))

@@ -67,7 +67,7 @@ def test_full_set_sampled_against_oracle(name, ns_steps, variant, projs):
     assert owner.status() == dmuon.OK
     for i in sample:
         s = shapes[i]
-        gram = variant == 1 and max(s) >= 2 * min(s)
+        gram = dmuon.ns_variant_for(s, ns_steps, variant) == dmuon.NS_GRAM
         m_ref, o_ref, w_ref = oracle.muon_step(g0[i], np.zeros(s), w0[i], lr=0.02, beta=0.95,
                                                ns_steps=ns_steps,
                                                variant="gram" if gram else "standard")

@@ -230,8 +230,8 @@ def test_gram_variant(dm, wl, steps):
     run_ns(dm, ps, steps, variant=dm.NS_GRAM)
     assert ps.guards_intact()
     for i, s in enumerate(shapes):
-        m, n = min(s), max(s)
-        ref = (oracle.gram_newton_schulz if n >= 2 * m else oracle.newton_schulz)(ins[i], steps)
+        gram = dm.ns_variant_for(s, steps, dm.NS_GRAM) == dm.NS_GRAM
+        ref = (oracle.gram_newton_schulz if gram else oracle.newton_schulz)(ins[i], steps)
         err = rel(np64(ps.view(i)), ref)
         assert err <= NS_TOL[steps], f"gram {s} steps={steps}: rel err {err:.3e}"
 
@@ -311,7 +311,8 @@ def _muon_case(dm, wl, shapes, gdt, wdt, steps=2, variant=0, seed=0, ns_steps=5)
         for i, s in enumerate(shapes):
             m_ref[i], o_ref, w_new = oracle.muon_step(
                 np64(gs[i]), m_ref[i], w_before[i], lr=0.02, beta=0.95, ns_steps=ns_steps,
-                variant="gram" if (variant == 1 and max(s) >= 2 * min(s)) else "standard")
+                variant="gram" if dm.ns_variant_for(s, ns_steps, variant) == dm.NS_GRAM
+                else "standard")
             assert rel(np64(ms[i]), m_ref[i]) <= 1e-5, f"momentum {s}"
             err_o = rel(np64(own.packed_view(i)), o_ref)
             assert err_o <= NS_TOL[ns_steps], f"step {step} {s}: O rel err {err_o:.3e}"
