@@ -229,7 +229,18 @@ def trace_summary(rec, step_ms: float):
         m = rec["launch"] == L
         spans.append((int(entry[m].min()), int(exit_[m].max())))
     gaps = sum(max(0, spans[k + 1][0] - spans[k][1]) for k in range(len(spans) - 1)) * 1e-6
+    # the leaders' MMA threads: share of their MMA span spent waiting, per product kind
+    waits = {}
+    if "mma_span_cycles" in rec:
+        names = {0: "sym_k", 1: "sym_mn", 2: "full_wide", 3: "full_tall"}
+        for kd, nm in names.items():
+            sel = has & (rec["kind"] == kd)
+            span = float(rec["mma_span_cycles"][sel].sum().item())
+            if span > 0:
+                waits[nm] = {"operand": float(rec["wait_operand_cycles"][sel].sum().item()) / span,
+                             "accumulator": float(rec["wait_accum_cycles"][sel].sum().item()) / span}
     return {"launches": len(launches), "pairs": pairs, "step_ms": step_ms,
+            "mma_thread_wait_frac": waits,
             "product_window_ms": window,
             "mma_active_frac": busy / total, "fill_drain_frac": (resident - busy) / total,
             "not_resident_frac": (total - resident) / total,

@@ -336,6 +336,12 @@ typedef struct {
   uint32_t kind;             /* product kind: 0 sym K-major, 1 sym MN-major, 2 full wide, 3 full tall */
   uint32_t tiles;            /* 256 x 256 tiles of the whole launch */
   uint64_t t_entry_ns, t_mma_first_ns, t_mma_last_ns, t_exit_ns;
+  /* first CTA of a pair, in SM cycles: its MMA thread's span (its start to the
+     drain of its last MMA), and within it the waits for operand stages and for the
+     epilogue to free an accumulator (0 elsewhere).  With the MMAs queued ahead of
+     the tensor pipe, operand waits include the normal run-ahead of the thread, so
+     they bound, not measure, operand starvation */
+  uint64_t mma_span_cycles, wait_operand_cycles, wait_accum_cycles;
 } dmuon_trace_record;
 int dmuon_trace_begin(void* records, size_t bytes);
 long long dmuon_trace_end(void);

@@ -63,7 +63,7 @@ constexpr int kBarBytes = 512;
 constexpr size_t kSmemBytes =
     size_t(kStages) * kStageBytes + kEpiBytes + 1024 + kBarBytes;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory above the sm_100 per-block limit");
-static_assert((2 * kStages + 5 + 2 * kEpiWarps) * 8 + 8 + 16 <= kBarBytes,
+static_assert((2 * kStages + 5 + 2 * kEpiWarps) * 8 + 8 + 40 <= kBarBytes,
               "barrier area too small");
 // After a bounded wait gives up, wait this long before leaving so that copies
 // and MMAs already issued to this CTA's shared memory / TMEM have landed.
@@ -217,6 +217,9 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
   constexpr uint32_t idesc = idesc_bf16(kTileM, kTileN, Kind<KIND>::l_mn, Kind<KIND>::r_mn);
   const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
   const int clusters = int(cluster_count_x());
+  const bool tracing = g.trace != nullptr;
+  long long wait_op = 0, wait_acc = 0;
+  const long long c_first = tracing ? clock64() : 0;
   int stage = 0;
   uint32_t phase = 0;
   int it = 0;
@@ -236,21 +239,25 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
     constexpr uint32_t b_kstep = Kind<KIND>::r_mn ? (2048u >> 4) : (32u >> 4);
     const int acc = it & 1;
     const uint32_t aph = uint32_t(it >> 1) & 1u;
+    const long long tw0 = tracing ? clock64() : 0;
     if (!mbar_wait_cluster(&tempty[acc], aph ^ 1u, abort_flag)) {
       raise_abort(g.err, abort_flag);
       break;
     }
+    if (tracing) wait_acc += clock64() - tw0;
     tc_fence_after();
     const uint32_t d = tmem_base + uint32_t(acc * kAccCols);
     bool ok = true;
     for (int kb = 0; kb < KB; ++kb) {
+      const long long tw1 = tracing ? clock64() : 0;
       if (!mbar_wait_cluster(&full_bar[stage], phase, abort_flag)) {
         raise_abort(g.err, abort_flag);
         ok = false;
         break;
       }
+      if (tracing) wait_op += clock64() - tw1;
       tc_fence_after();
-      if (g.trace != nullptr && tstamp[0] == 0) tstamp[0] = globaltimer_ns();
+      if (tracing && tstamp[0] == 0) tstamp[0] = globaltimer_ns();
       const uint64_t ad = a_desc + uint64_t(stage * (kAStage >> 4));
       const uint64_t bd = b_desc + uint64_t(stage * (kBStage >> 4));
 #pragma unroll
@@ -268,7 +275,12 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
   // Every issued MMA must finish before TMEM and shared memory go away.
   umma_commit_pair(drain_bar, 0x1);
   (void)mbar_wait(drain_bar, 0, nullptr);
-  if (g.trace != nullptr && tstamp[0] != 0) tstamp[1] = globaltimer_ns();
+  if (tracing && tstamp[0] != 0) {
+    tstamp[1] = globaltimer_ns();
+    tstamp[2] = (unsigned long long)wait_op;
+    tstamp[3] = (unsigned long long)wait_acc;
+    tstamp[4] = (unsigned long long)(clock64() - c_first);
+  }
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -559,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   uint64_t* aux_bar = drain_bar + 1;     // two per epilogue warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + 2 * kEpiWarps);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  // first / last MMA time of this CTA (traced launches only)
+  // first / last MMA time and the MMA thread's wait cycles (traced launches only)
   unsigned long long* tstamp = reinterpret_cast<unsigned long long*>(aux_bar + 2 * kEpiWarps + 1);
   const unsigned long long t_entry = g.trace != nullptr ? globaltimer_ns() : 0ull;
 
@@ -577,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     mbar_init(drain_bar, 1);
     for (int a = 0; a < 2 * kEpiWarps; ++a) mbar_init(&aux_bar[a], 1);  // lane 0's expect_tx
     *abort_flag = 0;
-    tstamp[0] = tstamp[1] = 0;
+    for (int k = 0; k < 5; ++k) tstamp[k] = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -621,6 +633,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     r.t_mma_first = tstamp[0];
     r.t_mma_last = tstamp[1];
     r.t_exit = globaltimer_ns();
+    r.mma_span_cycles = tstamp[4];
+    r.wait_operand_cycles = tstamp[2];
+    r.wait_accum_cycles = tstamp[3];
     g.trace[blockIdx.x] = r;
   }
 }

@@ -120,6 +120,10 @@ struct TraceRec {
   uint32_t kind;                 // ProductKind
   uint32_t tiles;                // tiles of the whole launch
   unsigned long long t_entry, t_mma_first, t_mma_last, t_exit;
+  // leader's MMA thread, in SM cycles: from its start to the drain of its last
+  // MMA, and within that the waits for operand stages to land and for an
+  // accumulator to be freed by the epilogue
+  unsigned long long mma_span_cycles, wait_operand_cycles, wait_accum_cycles;
 };
 
 // Launch arguments of the grouped Newton-Schulz product kernel.

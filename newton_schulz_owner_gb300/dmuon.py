@@ -85,7 +85,7 @@ _lib.dmuon_trace_begin.argtypes = [_vp, _sz]
 _lib.dmuon_trace_begin.restype = _i
 _lib.dmuon_trace_end.argtypes = []
 _lib.dmuon_trace_end.restype = ctypes.c_longlong
-TRACE_RECORD_BYTES = 48
+TRACE_RECORD_BYTES = 72
 
 
 class DMuonError(RuntimeError):
@@ -285,11 +285,12 @@ def trace_end(buffer):
     after the traced work has completed)."""
     n = int(_lib.dmuon_trace_end())
     raw = buffer[:n * TRACE_RECORD_BYTES].cpu()
-    u32 = raw.view(torch.int32).view(n, 12).to(torch.int64) & 0xFFFFFFFF
-    u64 = raw.view(torch.int64).view(n, 6)
+    u32 = raw.view(torch.int32).view(n, 18).to(torch.int64) & 0xFFFFFFFF
+    u64 = raw.view(torch.int64).view(n, 9)
     return {"launch": u32[:, 0], "cta": u32[:, 1], "kind": u32[:, 2], "tiles": u32[:, 3],
             "t_entry": u64[:, 2], "t_mma_first": u64[:, 3], "t_mma_last": u64[:, 4],
-            "t_exit": u64[:, 5]}
+            "t_exit": u64[:, 5], "mma_span_cycles": u64[:, 6], "wait_operand_cycles": u64[:, 7],
+            "wait_accum_cycles": u64[:, 8]}
 
 
 class MuonOwner:
