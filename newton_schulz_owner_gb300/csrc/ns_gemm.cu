@@ -359,6 +359,21 @@ DM_DEV void store_final_chunk(const GemmArgs& g, const Bucket& B, const TileInfo
   }
 }
 
+// One lane's 32 consecutive elements of row `row` of an m x m slot, columns
+// c0 .. c0 + 31 (four 16-byte loads; rows are 128-byte aligned and the row
+// pitch covers every such chunk), or zeros for a row beyond m.
+DM_DEV void load_row32(const __nv_bfloat16* base, int pitch, int m, int row, int c0,
+                       uint4 (&q)[4]) {
+  if (row < m) {
+    const uint4* src = reinterpret_cast<const uint4*>(base + (long long)row * pitch + c0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) q[u] = src[u];
+  } else {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) q[u] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 template <int KIND>
 DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t* tempty,
                      uint64_t* aux_bar_all, uint32_t epi_smem, uint32_t tmem_base,
@@ -406,12 +421,30 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
   }
   bool ok = true;
   int it = 0;
+  // symmetric products with beta != 0: this lane's row of the b*A operand for the
+  // current chunk, loaded one chunk ahead (the tile's first chunk while the
+  // accumulator is still being filled)
+  const bool sym_aux = !FULL && g.beta != 0.f;
+  uint4 a_cur[4];
   for (; ok && t < g.total_tiles; t += clusters, ++it) {
     const TileInfo T = decode_tile<KIND>(g, g.tile_base + t);
     const Bucket& B = g.buckets[T.bucket];
     if (lane == 0) acquire_maps(T.bucket, B);
     const int acc = it & 1;
     const uint32_t aph = uint32_t(it >> 1) & 1u;
+    // chunks of this warp in this tile: cc_lo .. cc_hi - 1 (the lower chunks of a
+    // diagonal tile are written as mirrors of upper ones; columns past the
+    // output are not written)
+    const int ncols_t = FULL && !Kind<KIND>::tall ? B.n : B.m;
+    int cc_lo = 0, cc_hi = 0;
+    while (cc_hi < 4 && T.tj * kTileN + h * 128 + cc_hi * 32 < ncols_t) ++cc_hi;
+    if (!FULL && T.ti == T.tj)
+      while (cc_lo < cc_hi && h * 128 + cc_lo * 32 < r_loc) ++cc_lo;
+    const __nv_bfloat16* a_base =
+        sym_aux ? B.slot[g.sAux] + (long long)T.mat * B.stride_m : nullptr;
+    if (sym_aux && cc_lo < cc_hi)
+      load_row32(a_base, B.pitch_m, B.m, T.ti * kTileM + r_loc + lane,
+                 T.tj * kTileN + h * 128 + cc_lo * 32, a_cur);
     int w = 1;
     if (lane == 0) w = mbar_wait_cluster(&tfull[acc], aph, abort_flag) ? 1 : 0;
     w = __shfl_sync(0xffffffffu, w, 0);
@@ -430,12 +463,9 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
     const bool diag_tile = !FULL && T.ti == T.tj;
     const void* out_map = emap_of(g, B, g.sOut);
 #pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
+    for (int cc = cc_lo; cc < cc_hi; ++cc) {
       const int c_loc = h * 128 + cc * 32;
       const int c0 = T.tj * kTileN + c_loc;
-      if (c0 >= ncols) break;  // warp-uniform
-      // lower chunks of a diagonal tile are written as mirrors of upper ones
-      if (diag_tile && c_loc < r_loc) continue;
       float v[32];
       tmem_ld32(tmem_base + uint32_t(acc * kAccCols + c_loc) + (uint32_t(q * 32) << 16), v);
       tmem_ld_wait();
@@ -483,27 +513,21 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
           issue_aux(T, B, cc + 2);
         }
       } else {
-        const int m = B.m;
-        // both buffers free of earlier stores
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
-        if (g.beta != 0.f) {
-          // beta*A: the 32 x 32 chunk of A comes in with 8 rows x 64 bytes per
-          // load instruction through buffer 1, then each lane takes its row
-          const __nv_bfloat16* A = B.slot[g.sAux] + (long long)T.mat * B.stride_m + c0;
-          const int u = lane & 3;
-#pragma unroll
-          for (int it = 0; it < 4; ++it) {
-            const int row = it * 8 + (lane >> 2);
-            uint4 q = make_uint4(0u, 0u, 0u, 0u);
-            if (rg0 + row < m)
-              q = *reinterpret_cast<const uint4*>(A + (long long)(rg0 + row) * B.pitch_m + u * 8);
-            st_shared_v4(buf(1) + epi_off(row, u), q.x, q.y, q.z, q.w);
-          }
-          __syncwarp();
+        if (sym_aux) {
+          // beta*A from this lane's row (loaded a chunk ahead); start the next
+          // chunk's row before using this one
           float a[32];
-          epi_load_row(buf(1), lane, a);
-          __syncwarp();  // buffer 1 is rewritten below
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t wv[4] = {a_cur[u].x, a_cur[u].y, a_cur[u].z, a_cur[u].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[k]));
+              a[8 * u + 2 * k] = f.x;
+              a[8 * u + 2 * k + 1] = f.y;
+            }
+          }
+          if (cc + 1 < cc_hi) load_row32(a_base, B.pitch_m, B.m, r, c0 + 32, a_cur);
 #pragma unroll
           for (int j = 0; j < 32; ++j) o[j] = fmaf(g.gamma, v[j], g.beta * a[j]);
         } else {
@@ -516,6 +540,9 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
           for (int j = 0; j < 32; ++j)
             if (j == d) o[j] += alpha;
         }
+        // both buffers free of earlier stores
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
         const bool diag_chunk = diag_tile && c_loc == r_loc;
         epi_store_row(buf(0), lane, o);
         if (diag_chunk) {
