@@ -503,18 +503,22 @@ def run_gpu(args, rank, world, local_rank):
     step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     barrier()
     dmuon.launch_count(reset=True)
+    torch.cuda.nvtx.range_push("whole_step")   # for profiler selection (ncu --nvtx-include)
     step_ev[0].record(stream)
     for k in range(args.steps):
         whole_step()
         step_ev[k + 1].record(stream)
+    torch.cuda.nvtx.range_pop()
     timed_launches = dmuon.launch_count(reset=True)   # the library's own count
     barrier()
     # timed region 2 -- the same step as its three calls (pack, Newton-Schulz,
     # update) with events between them: the per-phase times and the roofline
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     barrier()
+    torch.cuda.nvtx.range_push("three_call")
     for k in range(args.steps):
         step_phases(evs[k])
+    torch.cuda.nvtx.range_pop()
     barrier()
     clocks = sampler.stop()
     st = dmuon.stream_status(owner.workspace, stream)

@@ -42,7 +42,7 @@ struct BucketPlan {
   std::vector<int> sym;   // (ti << 16) | tj, upper-triangle tiles of an m x m product
   int full_ti = 0, full_tj = 0;
   int first = 0;                    // table position of the first matrix
-  long long chunk_lo = 0, chunks = 0, tile_lo = 0, tiles = 0;  // its elementwise work
+  long long chunk_lo = 0, chunks = 0;  // its elementwise chunks
   int sym_begin = 0, full_begin = 0;  // first product tile of the bucket within its group
 };
 
@@ -51,12 +51,12 @@ struct Plan {
   std::vector<BucketPlan> buckets;  // standard buckets first, then Gram buckets
   int n_std = 0;                    // number of standard buckets
   std::vector<int> bucket_of, idx_in_bucket, internal_of;
-  std::vector<long long> chunk_begin, tile_begin;  // per caller matrix
+  std::vector<long long> chunk_begin;              // per caller matrix
   std::vector<long long> partial_begin;            // per caller matrix, caller order
-  std::vector<int> n_chunks, tiles_r, tiles_c;     // per caller matrix
+  std::vector<int> n_chunks;                       // per caller matrix
   std::vector<int> ew_order;                        // table position -> caller matrix
   std::vector<int> ew_pos;                          // caller matrix -> table position
-  long long total_chunks = 0, total_tiles = 0;
+  long long total_chunks = 0;
   int n_internal = 0;
   int sym_total = 0;
   size_t off_tables = 0, tables_bytes = 0;
@@ -117,11 +117,8 @@ int build_plan(int n, const dmuon_shape* shp, int variant, int ns_steps, Plan& P
   P.idx_in_bucket.assign(n, -1);
   P.internal_of.assign(n, -1);
   P.chunk_begin.assign(n, 0);
-  P.tile_begin.assign(n, 0);
   P.partial_begin.assign(n, 0);
   P.n_chunks.assign(n, 0);
-  P.tiles_r.assign(n, 0);
-  P.tiles_c.assign(n, 0);
 
   // buckets keyed by (gram, m, n, tall); standard first, each group in
   // first-seen order
@@ -132,8 +129,6 @@ int build_plan(int n, const dmuon_shape* shp, int variant, int ns_steps, Plan& P
     if (!shape_ok(shp[i])) return DMUON_ERR_INVALID_ARG;
     const long long r = shp[i].rows, c = shp[i].cols;
     P.n_chunks[i] = int(ceil_div(r * c, kChunk));
-    P.tiles_r[i] = int(ceil_div(r, kRelayTile));
-    P.tiles_c[i] = int(ceil_div(c, kRelayTile));
     if (r == 0 || c == 0) continue;
     const int m = int(std::min(r, c)), nn = int(std::max(r, c));
     const Key key(uses_gram(variant, m, nn, ns_steps) ? 1 : 0, m, nn, r > c ? 1 : 0);
@@ -195,7 +190,7 @@ int build_plan(int n, const dmuon_shape* shp, int variant, int ns_steps, Plan& P
 
   // The per-matrix table follows the internal (bucket-major) order, empty
   // matrices last, so that every bucket -- and every run of buckets -- is one
-  // contiguous range of table entries, chunks and relayout tiles.
+  // contiguous range of table entries and elementwise chunks.
   P.ew_pos.assign(n, -1);
   for (const auto& B : P.buckets)
     for (int i : B.mats) P.ew_order.push_back(i);
@@ -210,9 +205,7 @@ int build_plan(int n, const dmuon_shape* shp, int variant, int ns_steps, Plan& P
     const int i = P.ew_order[k];
     P.ew_pos[i] = k;
     P.chunk_begin[i] = P.total_chunks;
-    P.tile_begin[i] = P.total_tiles;
     P.total_chunks += P.n_chunks[i];
-    P.total_tiles += (long long)P.tiles_r[i] * P.tiles_c[i];
   }
   // product tile numbering: one sequence over the standard buckets, another
   // over the Gram buckets (each group's launches start at its first bucket)
@@ -222,11 +215,7 @@ int build_plan(int n, const dmuon_shape* shp, int variant, int ns_steps, Plan& P
     if (int(b) == P.n_std) sym_begin = full_begin = 0;
     B.first = P.ew_pos[B.mats.front()];
     B.chunk_lo = P.chunk_begin[B.mats.front()];
-    B.tile_lo = P.tile_begin[B.mats.front()];
-    for (int i : B.mats) {
-      B.chunks += P.n_chunks[i];
-      B.tiles += (long long)P.tiles_r[i] * P.tiles_c[i];
-    }
+    for (int i : B.mats) B.chunks += P.n_chunks[i];
     B.sym_begin = int(sym_begin);
     B.full_begin = int(full_begin);
     sym_begin += (long long)B.mats.size() * (long long)B.sym.size();
@@ -469,10 +458,7 @@ int upload_tables(const Request& R, const Plan& P) {
     E.active = (r > 0 && c > 0) ? 1 : 0;
     E.chunk_begin = P.chunk_begin[i];
     E.partial_begin = P.partial_begin[i];
-    E.tile_begin = P.tile_begin[i];
     E.n_chunks = P.n_chunks[i];
-    E.tiles_r = P.tiles_r[i];
-    E.tiles_c = P.tiles_c[i];
     E.packed_off = E.active ? R.offset[i] : 0;
     E.upd_scale = float(std::sqrt(std::max(1.0, double(r) / double(std::max<long long>(c, 1)))));
     if (R.do_pack && E.active) {
@@ -697,7 +683,7 @@ constexpr double kMinPieceBytes = 64.0 * (1 << 20);
 enum PieceKind : int { kPiecePack = 0, kPieceFinalize = 1, kPieceRelayout = 2, kPieceUpdate = 3 };
 struct Piece {
   int kind = 0, bucket = 0;
-  long long lo = 0, hi = 0;  // chunk (pack, update) or tile (relayout) range within the bucket
+  long long lo = 0, hi = 0;  // chunk range within the bucket
 };
 
 struct StepSchedule {
@@ -717,12 +703,12 @@ double model_launch_seconds(const BucketPlan& B, int i) {
 }
 
 struct PieceCosts {
-  double pack_chunk, relay_tile, update_chunk;  // bytes moved per chunk / tile
+  double pack_chunk, relay_chunk, update_chunk;  // bytes moved per chunk
 };
 
 PieceCosts piece_costs(const Request& R) {
   const double g = R.grad_dt == DMUON_BF16 ? 2.0 : 4.0, w = R.weight_dt == DMUON_BF16 ? 2.0 : 4.0;
-  return {double(kChunk) * (g + 4.0 + 4.0 + 2.0), double(kRelayTile) * kRelayTile * 4.0,
+  return {double(kChunk) * (g + 4.0 + 4.0 + 2.0), double(kChunk) * 4.0,
           double(kChunk) * (2.0 + 2.0 * w)};
 }
 
@@ -751,7 +737,7 @@ StepSchedule plan_step(const Plan& P, const Request& R, const std::vector<int>& 
       if (!S.prepacked[k]) {
         mb.push_back({k, kPiecePack, 0, B.chunks});
         mb.push_back({k, kPieceFinalize, 0, 1});
-        mb.push_back({k, kPieceRelayout, 0, B.tiles});
+        mb.push_back({k, kPieceRelayout, 0, B.chunks});
       }
       upd.push_back({k, kPieceUpdate, 0, B.chunks});
     }
@@ -775,7 +761,7 @@ StepSchedule plan_step(const Plan& P, const Request& R, const std::vector<int>& 
         while (mi < mb.size()) {
           Todo& t = mb[mi];
           const double ub = t.kind == kPiecePack ? pc.pack_chunk
-                            : t.kind == kPieceRelayout ? pc.relay_tile : 0.0;
+                            : t.kind == kPieceRelayout ? pc.relay_chunk : 0.0;
           if (!take(t, ub)) break;
           ++mi;
         }
@@ -800,7 +786,7 @@ StepSchedule plan_step(const Plan& P, const Request& R, const std::vector<int>& 
   for (int k = 0; k < g; ++k) {
     const BucketPlan& B = P.buckets[ord[k]];
     if (S.prepacked[size_t(k)])
-      S.exposed += (double(B.chunks) * pc.pack_chunk + double(B.tiles) * pc.relay_tile) /
+      S.exposed += double(B.chunks) * (pc.pack_chunk + pc.relay_chunk) /
                    kModelHbmBytes;
   }
   for (const Piece& t : S.tail_update)
@@ -854,14 +840,12 @@ int run(const Request& R) {
   const int nb = int(P.buckets.size());
 
   // the whole table, and the part of it that belongs to buckets [b0, b1)
-  EwRange all{ew, R.n, 0, 0, P.total_chunks, 0, P.total_tiles};
+  EwRange all{ew, R.n, 0, 0, P.total_chunks};
   auto range_of = [&](int b0, int b1) {
-    EwRange r{ew + P.buckets[b0].first, 0, P.buckets[b0].first, P.buckets[b0].chunk_lo, 0,
-              P.buckets[b0].tile_lo, 0};
+    EwRange r{ew + P.buckets[b0].first, 0, P.buckets[b0].first, P.buckets[b0].chunk_lo, 0};
     for (int b = b0; b < b1; ++b) {
       r.n += int(P.buckets[b].mats.size());
       r.chunks += P.buckets[b].chunks;
-      r.tiles += P.buckets[b].tiles;
     }
     return r;
   };
@@ -918,11 +902,11 @@ int run(const Request& R) {
         case kPieceFinalize:
           return launch_norm_finalize(r, partials, R.eps, inv, x) == cudaSuccess;
         case kPieceRelayout: {
-          r.tile_base += pc.lo;
-          r.tiles = pc.hi - pc.lo;
+          r.chunk_base += pc.lo;
+          r.chunks = pc.hi - pc.lo;
           if (launch_relayout(r, packed, inv, x) != cudaSuccess) return false;
           // the bucket is ready for its products after its last relayout piece
-          if (pc.hi == P.buckets[pc.bucket].tiles &&
+          if (pc.hi == P.buckets[pc.bucket].chunks &&
               cudaEventRecord(ev.e[size_t(pos_of[size_t(pc.bucket)])], x) != cudaSuccess)
             return false;
           return true;

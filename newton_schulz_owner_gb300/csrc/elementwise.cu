@@ -5,7 +5,7 @@
 //   norm_partials   the same partial sums from bf16 values already packed
 //   norm_finalize   inv_i = 1 / (sqrt(sum of matrix i's partials) + eps), fp64
 //   relayout        X0 = U * inv into the working layout (the parameter's own
-//                   orientation, rows padded to the slot pitch)
+//                   orientation, rows padded to the slot pitch): a chunked copy
 //   scale_inplace   packed <- bf16(U * inv)  (ns_steps = 0)
 //   update          W <- W - lr * sqrt(max(1, rows/cols)) * O
 // Every kernel reads and writes 16-byte vectors where the pointers allow and
@@ -24,14 +24,12 @@ constexpr int kVec = 8;                                   // elements per thread
 constexpr int kIters = kChunk / (kVec * kEwThreads);      // 4
 static_assert(kChunk == kVec * kEwThreads * kIters, "chunk shape");
 
-// Largest i with key(ew[i]) <= x (ew sorted by key).
-template <bool TILES>
-DM_DEV int find_mat(const EwMat* ew, int n, long long x) {
+// Largest i with ew[i].chunk_begin <= chunk (ew sorted by chunk_begin).
+DM_DEV int find_mat(const EwMat* ew, int n, long long chunk) {
   int lo = 0, hi = n - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    const long long b = TILES ? ew[mid].tile_begin : ew[mid].chunk_begin;
-    if (b <= x) lo = mid;
+    if (ew[mid].chunk_begin <= chunk) lo = mid;
     else hi = mid - 1;
   }
   return lo;
@@ -75,7 +73,7 @@ DM_DEV float block_sum(float v) {
 }
 
 // Every chunked kernel below works on the sub-range ew[0, n) of the per-matrix
-// table; `base` is the global index of its first chunk (tile for relayout).
+// table; `base` is the global index of its first chunk.
 template <bool G_BF16>
 __global__ void __launch_bounds__(kEwThreads) momentum_pack_kernel(const EwMat* __restrict__ ew,
                                                                    int n, long long base,
@@ -83,7 +81,7 @@ __global__ void __launch_bounds__(kEwThreads) momentum_pack_kernel(const EwMat* 
                                                                    __nv_bfloat16* packed,
                                                                    float* partials) {
   const long long chunk = base + blockIdx.x;
-  const EwMat& E = ew[find_mat<false>(ew, n, chunk)];
+  const EwMat& E = ew[find_mat(ew, n, chunk)];
   const long long start = (chunk - E.chunk_begin) * kChunk;
   const long long end = min(E.numel, start + kChunk);
   const float omb = 1.f - beta;
@@ -154,7 +152,7 @@ __global__ void __launch_bounds__(kEwThreads) norm_partials_kernel(const EwMat* 
                                                                    const __nv_bfloat16* packed,
                                                                    float* partials) {
   const long long chunk = base + blockIdx.x;
-  const EwMat& E = ew[find_mat<false>(ew, n, chunk)];
+  const EwMat& E = ew[find_mat(ew, n, chunk)];
   const long long start = (chunk - E.chunk_begin) * kChunk;
   const long long end = min(E.numel, start + kChunk);
   const __nv_bfloat16* P = packed + E.packed_off;
@@ -198,36 +196,45 @@ __global__ void __launch_bounds__(kEwThreads) norm_finalize_kernel(const EwMat* 
 }
 
 // X0 = U * inv into the working layout: the parameter's own orientation with
-// rows padded to the slot pitch.  One block per 64 x 64 tile of the parameter;
-// each thread copies 16 consecutive elements of one row.
+// rows padded to the slot pitch.  One block per chunk of the packed matrix, read
+// in its row-major order like every other chunked kernel; where cols % 8 == 0
+// each thread moves 16-byte vectors, none of which crosses a row, to
+// row * pitch + col.
 __global__ void __launch_bounds__(kEwThreads) relayout_kernel(const EwMat* __restrict__ ew, int n,
                                                               long long base,
                                                               const __nv_bfloat16* packed,
                                                               const float* inv_norm) {
-  const long long t = base + blockIdx.x;
-  const int i = find_mat<true>(ew, n, t);
+  const long long chunk = base + blockIdx.x;
+  const int i = find_mat(ew, n, chunk);
   const EwMat& E = ew[i];
-  const long long local = t - E.tile_begin;
-  const int tr = int(local / E.tiles_c), tc = int(local % E.tiles_c);
-  const int r = tr * kRelayTile + (threadIdx.x >> 2);
-  const int c0 = tc * kRelayTile + (threadIdx.x & 3) * 16;
-  const int rows = E.rows, cols = E.cols;
-  if (r >= rows || c0 >= cols) return;
+  const long long start = (chunk - E.chunk_begin) * kChunk;
+  const long long end = min(E.numel, start + kChunk);
   const float inv = inv_norm[i];
-  const __nv_bfloat16* src = packed + E.packed_off + (long long)r * cols + c0;
-  __nv_bfloat16* dst = E.x0 + (long long)r * E.pitch_x + c0;
-  const int cnt = min(16, cols - c0);
-  if (cnt == 16 && (E.flags & kFlagRowsAligned)) {
+  const __nv_bfloat16* P = packed + E.packed_off;
+  __nv_bfloat16* X = E.x0;
+  const long long cols = E.cols, pitch = E.pitch_x;
+  if (E.flags & kFlagRowsAligned) {
 #pragma unroll
-    for (int v = 0; v < 2; ++v) {
-      float f[8];
-      bf16x8_to_f32(reinterpret_cast<const uint4*>(src)[v], f);
+    for (int it = 0; it < kIters; ++it) {
+      const long long e = start + (long long)(it * kEwThreads + threadIdx.x) * kVec;
+      if (e >= end) break;
+      const long long r = e / cols, c = e - r * cols;
+      float f[kVec];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(P + e), f);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) f[k] *= inv;
-      reinterpret_cast<uint4*>(dst)[v] = f32x8_to_bf16x8(f);
+      for (int k = 0; k < kVec; ++k) f[k] *= inv;
+      *reinterpret_cast<uint4*>(X + r * pitch + c) = f32x8_to_bf16x8(f);
     }
   } else {
-    for (int k = 0; k < cnt; ++k) dst[k] = __float2bfloat16_rn(__bfloat162float(src[k]) * inv);
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+      const long long e0 = start + (long long)(it * kEwThreads + threadIdx.x) * kVec;
+      if (e0 >= end) break;
+      for (int k = 0; k < kVec && e0 + k < end; ++k) {
+        const long long e = e0 + k, r = e / cols, c = e - r * cols;
+        X[r * pitch + c] = __float2bfloat16_rn(__bfloat162float(P[e]) * inv);
+      }
+    }
   }
 }
 
@@ -236,7 +243,7 @@ __global__ void __launch_bounds__(kEwThreads) scale_inplace_kernel(const EwMat* 
                                                                    __nv_bfloat16* packed,
                                                                    const float* inv_norm) {
   const long long chunk = base + blockIdx.x;
-  const int i = find_mat<false>(ew, n, chunk);
+  const int i = find_mat(ew, n, chunk);
   const EwMat& E = ew[i];
   const long long start = (chunk - E.chunk_begin) * kChunk;
   const long long end = min(E.numel, start + kChunk);
@@ -264,7 +271,7 @@ __global__ void __launch_bounds__(kEwThreads) update_kernel(const EwMat* __restr
                                                             long long base, float lr,
                                                             const __nv_bfloat16* packed) {
   const long long chunk = base + blockIdx.x;
-  const EwMat& E = ew[find_mat<false>(ew, n, chunk)];
+  const EwMat& E = ew[find_mat(ew, n, chunk)];
   const long long start = (chunk - E.chunk_begin) * kChunk;
   const long long end = min(E.numel, start + kChunk);
   const float coef = -(lr * E.upd_scale);
@@ -474,9 +481,9 @@ cudaError_t launch_norm_finalize(const EwRange& r, const float* partials, float 
 
 cudaError_t launch_relayout(const EwRange& r, const __nv_bfloat16* packed, const float* inv_norm,
                             cudaStream_t s) {
-  if (r.tiles <= 0) return cudaSuccess;
-  relayout_kernel<<<grid_of(r.tiles), kEwThreads, 0, s>>>(r.ew, r.n, r.tile_base, packed,
-                                                          inv_norm + r.first);
+  if (r.chunks <= 0) return cudaSuccess;
+  relayout_kernel<<<grid_of(r.chunks), kEwThreads, 0, s>>>(r.ew, r.n, r.chunk_base, packed,
+                                                           inv_norm + r.first);
   return counted(cudaGetLastError());
 }
 

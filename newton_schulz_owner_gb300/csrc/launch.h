@@ -35,13 +35,12 @@ cudaError_t launch_diag_shift(const Bucket* buckets, int n_buckets, int first_in
 // kernel parameters (stream-ordered, no host staging, no allocation).
 cudaError_t launch_upload(void* dst, const void* src, size_t bytes, cudaStream_t s);
 // A contiguous range of the per-matrix table: ew[0, n) are entries first ..
-// first + n - 1 (device pointer to entry `first`); their elementwise chunks are
-// [chunk_base, chunk_base + chunks) and their relayout tiles
-// [tile_base, tile_base + tiles).
+// first + n - 1 (device pointer to entry `first`); the kernel works on the
+// elementwise chunks [chunk_base, chunk_base + chunks) of those matrices.
 struct EwRange {
   const EwMat* ew;
   int n, first;
-  long long chunk_base, chunks, tile_base, tiles;
+  long long chunk_base, chunks;
 };
 cudaError_t launch_momentum_pack(const EwRange& r, bool grad_bf16, float beta,
                                  __nv_bfloat16* packed, float* partials, cudaStream_t s);

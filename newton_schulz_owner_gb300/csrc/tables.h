@@ -6,12 +6,11 @@
 
 namespace dm {
 
-// Elementwise kernels (momentum + pack, norm partials, update) walk each
-// matrix in chunks of kChunk elements; one block per chunk.
+// Elementwise kernels (momentum + pack, norm partials, relayout, update) walk
+// each matrix in chunks of kChunk elements of its row-major order; one block
+// per chunk.
 constexpr int kChunk = 8192;
 constexpr int kEwThreads = 256;
-// Relayout (normalise into the working layout, a padded-pitch copy): 64x64 tiles.
-constexpr int kRelayTile = 64;
 
 // Per-bucket buffers.  Slots 0-1 hold m x n working matrices X, slots 2-7 hold
 // m x m matrices (A, B for standard Newton-Schulz; A, P, Q, T for Gram).
@@ -41,10 +40,8 @@ struct EwMat {
                            // partials' layout does not depend on the variant
                            // (a pack and a later Newton-Schulz call may plan
                            // their buckets differently)
-  long long tile_begin;    // first relayout tile
   int rows, cols;
   int n_chunks;
-  int tiles_r, tiles_c;    // relayout tile grid over (rows, cols)
   int pitch_x;             // row pitch of the working layout (elements); the layout
                            // keeps the parameter's orientation (Y = X^T when rows > cols)
   int flags;
