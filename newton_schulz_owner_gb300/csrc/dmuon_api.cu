@@ -656,25 +656,29 @@ bool ns_gram(const GemmLauncher& L, const Request& R) {
 }
 
 // ------------------------------------------------------------------ step pipeline
-// The whole standard step overlaps its memory-bound work (momentum + pack,
-// norm finish and relayout of later buckets; weight update of earlier ones)
-// with the tensor-core products of the current bucket, on a second,
-// low-priority stream.  That work is enqueued in pieces, each one gated to
-// start together with one long product launch and sized to finish inside it:
-// a product launch ready to start while a memory-bound grid still has blocks
-// pending waits until that whole grid is dispatched (an SM filled with
-// memory-bound blocks has no room for a product CTA, about 38k registers, and
-// the block scheduler keeps refilling it from the pending grid), whereas
-// memory-bound blocks enqueued next to a resident product launch run in the
-// room its CTAs leave and never hold up the next launch.  What cannot be
-// placed runs on the caller's stream at full speed: the packs of the first
-// buckets before any product, the last bucket's update after all of them.
+// The whole standard step runs its buckets in positions -- a position is a run
+// of buckets (consecutive in the plan) whose products share launches -- and
+// overlaps its memory-bound work (momentum + pack, norm finish and relayout of
+// later positions; weight update of earlier ones) with the tensor-core
+// products of the current position, on a second, low-priority stream.  That
+// work is enqueued in pieces, each one gated to start together with one long
+// product launch and sized to finish inside it: a product launch ready to
+// start while a memory-bound grid still has blocks pending waits until that
+// whole grid is dispatched (an SM filled with memory-bound blocks has no room
+// for a product CTA, about 38k registers, and the block scheduler keeps
+// refilling it from the pending grid), whereas memory-bound blocks enqueued
+// next to a resident product launch run in the room its CTAs leave and never
+// hold up the next launch.  What cannot be placed runs on the caller's stream
+// at full speed: the packs of the first positions before any product, the
+// last position's update after all of them.
 //
-// Time model (only relative times matter): products at kModelTensorFlops
-// (algorithmic), memory-bound work at kModelHbmBytes alone and at
-// kModelCoBytes next to a product launch, of which a piece may plan to use
-// kSlotFill.
-constexpr double kModelTensorFlops = 1.55e15;
+// Time model (for choosing and sizing, not for results): a product launch
+// takes its busiest CTA pair's share of tile work (tiles go round-robin to the
+// pairs) at kModelPairFlops, plus kModelLaunchSeconds; memory-bound work moves
+// kModelHbmBytes alone and kModelCoBytes next to a product launch, of which a
+// piece may plan to use kSlotFill.
+constexpr double kModelPairFlops = 2.2e13;
+constexpr double kModelLaunchSeconds = 2e-5;
 constexpr double kModelHbmBytes = 6.5e12;
 constexpr double kModelCoBytes = 3.0e12;
 constexpr double kSlotFill = 0.45;
@@ -687,19 +691,50 @@ struct Piece {
 };
 
 struct StepSchedule {
-  std::vector<int> ord;                               // bucket order of the products
+  std::vector<std::pair<int, int>> pos;               // bucket range [b0, b1) of each position
   std::vector<char> prepacked;                        // per position: packed on `s` first
-  std::vector<std::vector<std::vector<Piece>>> slot;  // [position][launch]: pieces next to it
+  std::vector<std::vector<Piece>> slot;               // [position * launches + i]: pieces next to it
   std::vector<Piece> tail_update;                     // update ranges run on `s` at the end
-  double exposed = 0.0;                               // modelled seconds not hidden
+  double products = 0.0, exposed = 0.0;               // modelled seconds
 };
 
-// Modelled seconds of product launch i (= 3*step + phase) of bucket B.
-double model_launch_seconds(const BucketPlan& B, int i) {
-  const double m = B.m, n = B.n, cnt = double(B.mats.size());
+// Modelled seconds of product phase i (= 3*step + {X X^T, A A, B X}) over the
+// buckets [b0, b1): one launch per run of buckets of one orientation, as the
+// launcher issues them.
+double model_phase_seconds(const Plan& P, int b0, int b1, int i, int clusters) {
   const int phase = i % 3;
-  const double f = phase == 0 ? m * m * n : phase == 1 ? m * m * m : 2.0 * m * m * n;
-  return cnt * f / kModelTensorFlops;
+  double total = 0.0;
+  std::vector<double> load;
+  int b = b0;
+  while (b < b1) {
+    int e = b + 1;
+    while (e < b1 && P.buckets[e].tall == P.buckets[b].tall) ++e;
+    long long tiles = 0;
+    for (int k = b; k < e; ++k) {
+      const BucketPlan& B = P.buckets[k];
+      tiles += (long long)B.mats.size() *
+               (phase == 2 ? (long long)B.full_ti * B.full_tj : (long long)B.sym.size());
+    }
+    const int C = int(std::min<long long>(tiles, clusters));
+    if (C > 0) {
+      load.assign(size_t(C), 0.0);
+      long long first = 0;
+      for (int k = b; k < e; ++k) {
+        const BucketPlan& B = P.buckets[k];
+        const long long n = (long long)B.mats.size() *
+                            (phase == 2 ? (long long)B.full_ti * B.full_tj : (long long)B.sym.size());
+        const double K = phase == 0 ? double(B.n) : double(B.m);
+        const double cost = 2.0 * kTileM * kTileN * K;
+        const long long q = n / C, rem = n % C;
+        for (int c = 0; c < C; ++c) load[size_t(c)] += double(q) * cost;
+        for (long long r = 0; r < rem; ++r) load[size_t((first + r) % C)] += cost;
+        first += n;
+      }
+      total += *std::max_element(load.begin(), load.end()) / kModelPairFlops + kModelLaunchSeconds;
+    }
+    b = e;
+  }
+  return total;
 }
 
 struct PieceCosts {
@@ -712,48 +747,58 @@ PieceCosts piece_costs(const Request& R) {
           double(kChunk) * (2.0 + 2.0 * w)};
 }
 
-// Greedy placement for one bucket order.  Slots are the product launches in
-// issue order; each takes, up to its budget, first the pack/relayout work of
-// the nearest later bucket (needed before that bucket's products start), then
-// the updates of earlier buckets.  A bucket whose pack cannot be finished in
-// the slots before its products is packed on `s` up front instead, and the
-// placement is redone.
-StepSchedule plan_step(const Plan& P, const Request& R, const std::vector<int>& ord) {
-  const int g = int(ord.size());
+// Greedy placement for one sequence of positions.  Slots are the product
+// phases in issue order; each takes, up to its budget, first the pack/relayout
+// work of the nearest later position (needed before that position's products
+// start), then the updates of earlier positions.  A position whose pack cannot
+// be finished in the slots before its products is packed on `s` up front
+// instead, and the placement is redone.
+StepSchedule plan_step(const Plan& P, const Request& R,
+                       const std::vector<std::pair<int, int>>& pos, int clusters) {
+  const int g = int(pos.size());
   const int launches = 3 * R.ns_steps;
   const PieceCosts pc = piece_costs(R);
   StepSchedule S;
-  S.ord = ord;
+  S.pos = pos;
   S.prepacked.assign(size_t(g), 0);
   S.prepacked[0] = 1;
-  for (;;) {
-    S.slot.assign(size_t(g), std::vector<std::vector<Piece>>(size_t(launches)));
-    S.tail_update.clear();
-    // remaining work, as (position, kind, next unit, end unit)
-    struct Todo { int pos, kind; long long lo, hi; };
-    std::vector<Todo> mb, upd;
-    for (int k = 0; k < g; ++k) {
-      const BucketPlan& B = P.buckets[ord[k]];
-      if (!S.prepacked[k]) {
-        mb.push_back({k, kPiecePack, 0, B.chunks});
-        mb.push_back({k, kPieceFinalize, 0, 1});
-        mb.push_back({k, kPieceRelayout, 0, B.chunks});
-      }
-      upd.push_back({k, kPieceUpdate, 0, B.chunks});
+  std::vector<double> dur(size_t(g) * size_t(launches));
+  S.products = 0.0;
+  for (int k = 0; k < g; ++k)
+    for (int i = 0; i < launches; ++i) {
+      dur[size_t(k) * size_t(launches) + size_t(i)] =
+          model_phase_seconds(P, pos[size_t(k)].first, pos[size_t(k)].second, i, clusters);
+      S.products += dur[size_t(k) * size_t(launches) + size_t(i)];
     }
+  for (;;) {
+    S.slot.assign(size_t(g) * size_t(launches), std::vector<Piece>());
+    S.tail_update.clear();
+    struct Todo { int pos, kind, bucket; long long lo, hi; };
+    std::vector<Todo> mb, upd;
+    for (int k = 0; k < g; ++k)
+      for (int b = pos[size_t(k)].first; b < pos[size_t(k)].second; ++b) {
+        const long long ch = P.buckets[b].chunks;
+        if (!S.prepacked[size_t(k)]) {
+          mb.push_back({k, kPiecePack, b, 0, ch});
+          mb.push_back({k, kPieceFinalize, b, 0, 1});
+          mb.push_back({k, kPieceRelayout, b, 0, ch});
+        }
+        upd.push_back({k, kPieceUpdate, b, 0, ch});
+      }
     size_t mi = 0, ui = 0;
     int fail = -1;
     for (int k = 0; k < g && fail < 0; ++k) {
-      // every later bucket's pack must be done before its products start
+      // every later position's pack must be done before its products start
       if (mi < mb.size() && mb[mi].pos <= k) fail = mb[mi].pos;
       for (int i = 0; i < launches && fail < 0; ++i) {
-        double budget = model_launch_seconds(P.buckets[ord[k]], i) * kModelCoBytes * kSlotFill;
+        double budget = dur[size_t(k) * size_t(launches) + size_t(i)] * kModelCoBytes * kSlotFill;
         if (budget < kMinPieceBytes) continue;
+        std::vector<Piece>& out = S.slot[size_t(k) * size_t(launches) + size_t(i)];
         auto take = [&](Todo& t, double unit_bytes) {
           const long long can = unit_bytes > 0 ? (long long)(budget / unit_bytes) : t.hi - t.lo;
           const long long n = std::min(can, t.hi - t.lo);
           if (n <= 0) return false;
-          S.slot[size_t(k)][size_t(i)].push_back({t.kind, ord[t.pos], t.lo, t.lo + n});
+          out.push_back({t.kind, t.bucket, t.lo, t.lo + n});
           budget -= double(n) * unit_bytes;
           t.lo += n;
           return t.lo == t.hi;
@@ -772,26 +817,69 @@ StepSchedule plan_step(const Plan& P, const Request& R, const std::vector<int>& 
       }
     }
     if (fail < 0 && mi < mb.size()) fail = mb[mi].pos;
-    if (fail >= 0) {  // pack that bucket up front and place again
+    if (fail >= 0) {  // pack that position up front and place again
       S.prepacked[size_t(fail)] = 1;
       continue;
     }
     // updates left over (the unplaced rest of each) run on `s` after the last products
     for (; ui < upd.size(); ++ui)
       if (upd[ui].lo < upd[ui].hi)
-        S.tail_update.push_back({kPieceUpdate, ord[upd[ui].pos], upd[ui].lo, upd[ui].hi});
+        S.tail_update.push_back({kPieceUpdate, upd[ui].bucket, upd[ui].lo, upd[ui].hi});
     break;
   }
   S.exposed = 0.0;
-  for (int k = 0; k < g; ++k) {
-    const BucketPlan& B = P.buckets[ord[k]];
+  for (int k = 0; k < g; ++k)
     if (S.prepacked[size_t(k)])
-      S.exposed += double(B.chunks) * (pc.pack_chunk + pc.relay_chunk) /
-                   kModelHbmBytes;
-  }
+      for (int b = pos[size_t(k)].first; b < pos[size_t(k)].second; ++b)
+        S.exposed += double(P.buckets[b].chunks) * (pc.pack_chunk + pc.relay_chunk) /
+                     kModelHbmBytes;
   for (const Piece& t : S.tail_update)
     S.exposed += double(t.hi - t.lo) * pc.update_chunk / kModelHbmBytes;
   return S;
+}
+
+// The candidate schedules of a whole step: one position per bucket, by size
+// (short first products, small up-front packs), the same with the second
+// position moved last (the last position's update is exposed), and one
+// position per orientation (wide/square buckets, tall buckets; fewer, fuller
+// launches for sets of small matrices).  The one with the least modelled
+// product plus exposed time runs.
+StepSchedule choose_step_schedule(const Plan& P, const Request& R, int clusters) {
+  const int nb = int(P.buckets.size());
+  std::vector<int> ord(static_cast<size_t>(nb));
+  for (int b = 0; b < nb; ++b) ord[size_t(b)] = b;
+  std::stable_sort(ord.begin(), ord.end(), [&](int a, int b) {
+    return P.buckets[a].chunks < P.buckets[b].chunks;
+  });
+  std::vector<std::vector<std::pair<int, int>>> cands;
+  std::vector<std::pair<int, int>> one;
+  for (int b : ord) one.push_back({b, b + 1});
+  cands.push_back(one);
+  if (nb >= 3) {
+    std::vector<std::pair<int, int>> alt = one;
+    const auto second = alt[1];
+    alt.erase(alt.begin() + 1);
+    alt.push_back(second);
+    cands.push_back(alt);
+  }
+  int n_wide = 0;
+  while (n_wide < nb && !P.buckets[n_wide].tall) ++n_wide;
+  if (n_wide > 0 && n_wide < nb && nb > 2) {
+    long long cw = 0, ct = 0;
+    for (int b = 0; b < nb; ++b) (b < n_wide ? cw : ct) += P.buckets[b].chunks;
+    if (cw <= ct) cands.push_back({{0, n_wide}, {n_wide, nb}});
+    else cands.push_back({{n_wide, nb}, {0, n_wide}});
+  }
+  StepSchedule best;
+  bool have = false;
+  for (const auto& c : cands) {
+    StepSchedule S = plan_step(P, R, c, clusters);
+    if (!have || S.products + S.exposed < best.products + best.exposed) {
+      best = std::move(S);
+      have = true;
+    }
+  }
+  return best;
 }
 
 // Events used to order the two streams of an overlapped step; released when
@@ -851,46 +939,32 @@ int run(const Request& R) {
   };
 
   // A whole standard step over two or more buckets overlaps its memory-bound
-  // work with the products (see plan_step).  Candidate bucket orders: smallest
-  // first (short first products, small up-front packs), and the same with the
-  // smallest of the later buckets moved last (the last bucket's update is
-  // exposed); the one with less modelled exposed time runs.
+  // work with the products (see choose_step_schedule and plan_step).
   const bool overlap = R.do_pack && R.do_ns && R.do_update && R.ns_steps > 0 && P.n_std >= 2 &&
                        P.n_std == nb && D.aux != nullptr;
   if (overlap) {
-    std::vector<int> ord(static_cast<size_t>(nb));
-    for (int b = 0; b < nb; ++b) ord[size_t(b)] = b;
-    std::stable_sort(ord.begin(), ord.end(), [&](int a, int b) {
-      return P.buckets[a].chunks < P.buckets[b].chunks;
-    });
-    StepSchedule S = plan_step(P, R, ord);
-    if (nb >= 3) {
-      std::vector<int> alt = ord;
-      const int b = alt[1];
-      alt.erase(alt.begin() + 1);
-      alt.push_back(b);
-      StepSchedule T = plan_step(P, R, alt);
-      if (T.exposed < S.exposed) S = std::move(T);
-    }
+    const StepSchedule S = choose_step_schedule(P, R, D.max_clusters);
+    const int g = int(S.pos.size());
+    const int launches = 3 * R.ns_steps;
     cudaStream_t x = aux_stream_for(D, s);
     size_t n_slots = 0;
-    for (const auto& v : S.slot)
-      for (const auto& w : v) n_slots += w.empty() ? 0 : 1;
-    EventSet ev;  // [0, nb): position k's pack done on aux; nb: aux done; then one per used slot
-    if (!ev.create(nb + 1 + int(n_slots))) return DMUON_ERR_CUDA;
-    size_t next_ev = size_t(nb) + 1;
+    for (const auto& v : S.slot) n_slots += v.empty() ? 0 : 1;
+    EventSet ev;  // [0, g): position k's pack done on aux; g: aux done; then one per used slot
+    if (!ev.create(g + 1 + int(n_slots))) return DMUON_ERR_CUDA;
+    size_t next_ev = size_t(g) + 1;
     auto bucket_range = [&](int b) { return range_of(b, b + 1); };
+    std::vector<int> pos_of(static_cast<size_t>(nb), 0);
+    for (int k = 0; k < g; ++k)
+      for (int b = S.pos[size_t(k)].first; b < S.pos[size_t(k)].second; ++b) pos_of[size_t(b)] = k;
     // packs up front, on `s`, at full speed
-    for (int k = 0; k < nb; ++k) {
+    for (int k = 0; k < g; ++k) {
       if (!S.prepacked[size_t(k)]) continue;
-      const EwRange r = bucket_range(S.ord[size_t(k)]);
+      const EwRange r = range_of(S.pos[size_t(k)].first, S.pos[size_t(k)].second);
       if (launch_momentum_pack(r, gbf16, R.beta, packed, partials, s) != cudaSuccess ||
           launch_norm_finalize(r, partials, R.eps, inv, s) != cudaSuccess ||
           launch_relayout(r, packed, inv, s) != cudaSuccess)
         return DMUON_ERR_CUDA;
     }
-    std::vector<int> pos_of(static_cast<size_t>(nb), 0);
-    for (int k = 0; k < nb; ++k) pos_of[size_t(S.ord[size_t(k)])] = k;
     // one piece on the aux stream
     auto run_piece = [&](const Piece& pc) {
       EwRange r = bucket_range(pc.bucket);
@@ -905,9 +979,11 @@ int run(const Request& R) {
           r.chunk_base += pc.lo;
           r.chunks = pc.hi - pc.lo;
           if (launch_relayout(r, packed, inv, x) != cudaSuccess) return false;
-          // the bucket is ready for its products after its last relayout piece
-          if (pc.hi == P.buckets[pc.bucket].chunks &&
-              cudaEventRecord(ev.e[size_t(pos_of[size_t(pc.bucket)])], x) != cudaSuccess)
+          // the position is ready for its products after the last relayout piece
+          // of its last bucket
+          const int k = pos_of[size_t(pc.bucket)];
+          if (pc.hi == P.buckets[pc.bucket].chunks && pc.bucket + 1 == S.pos[size_t(k)].second &&
+              cudaEventRecord(ev.e[size_t(k)], x) != cudaSuccess)
             return false;
           return true;
         }
@@ -917,12 +993,11 @@ int run(const Request& R) {
           return launch_update(r, wbf16, R.lr, packed, x) == cudaSuccess;
       }
     };
-    for (int k = 0; k < nb; ++k) {
+    for (int k = 0; k < g; ++k) {
       if (!S.prepacked[size_t(k)] && cudaStreamWaitEvent(s, ev.e[size_t(k)], 0) != cudaSuccess)
         return DMUON_ERR_CUDA;
-      const auto& slots = S.slot[size_t(k)];
       auto before = [&](int i) {
-        const auto& pieces = slots[size_t(i)];
+        const auto& pieces = S.slot[size_t(k) * size_t(launches) + size_t(i)];
         if (pieces.empty()) return true;
         // the pieces start together with this product launch
         cudaEvent_t e = ev.e[next_ev++];
@@ -932,8 +1007,8 @@ int run(const Request& R) {
           if (!run_piece(pc)) return false;
         return true;
       };
-      if (!ns_standard(GemmLauncher(P, R, D.max_clusters, ws, S.ord[size_t(k)],
-                                    S.ord[size_t(k)] + 1, s),
+      if (!ns_standard(GemmLauncher(P, R, D.max_clusters, ws, S.pos[size_t(k)].first,
+                                    S.pos[size_t(k)].second, s),
                        R, P, ws, before))
         return DMUON_ERR_CUDA;
     }
@@ -945,8 +1020,8 @@ int run(const Request& R) {
     }
     // join: only if anything ran on the aux stream (under stream capture, an
     // aux stream that never forked from `s` is not part of the capture)
-    if (n_slots > 0 && (cudaEventRecord(ev.e[size_t(nb)], x) != cudaSuccess ||
-                        cudaStreamWaitEvent(s, ev.e[size_t(nb)], 0) != cudaSuccess))
+    if (n_slots > 0 && (cudaEventRecord(ev.e[size_t(g)], x) != cudaSuccess ||
+                        cudaStreamWaitEvent(s, ev.e[size_t(g)], 0) != cudaSuccess))
       return DMUON_ERR_CUDA;
     return DMUON_OK;
   }

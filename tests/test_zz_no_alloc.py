@@ -115,3 +115,38 @@ def test_noalloc_refuses_problems_beyond_its_scratch(dm):
     assert st == dm.ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.equal(packed, before)
+
+
+def test_noalloc_gram_variant_equals_workspace_call(dm):
+    """The same call with the Gram variant: the rule gives the rectangular
+    matrices the Gram form and the square one the standard form, in the built-in
+    array exactly as in a caller workspace (bit for bit), each within the
+    tolerance of the oracle's form for it."""
+    from newton_schulz_owner_gb300 import workloads as wl
+    shapes = [(128, 512), (512, 128), (200, 700), (256, 256), (96, 900)]
+    assert dm.ns_variant_for((128, 512), 5, dm.NS_GRAM) == dm.NS_GRAM
+    _, offsets, owner_elems = dm.plan(shapes)
+    assert dm.workspace_bytes(shapes, dm.NS_GRAM) <= dm.NOALLOC_SCRATCH_BYTES
+    ws = torch.zeros(dm.workspace_bytes(shapes, dm.NS_GRAM), dtype=torch.uint8, device="cuda")
+    ref = torch.zeros(sum(owner_elems), dtype=torch.bfloat16, device="cuda")
+    ins = []
+    for i, (r, c) in enumerate(shapes):
+        u = wl.random_matrix((r, c), 77 + i, "cuda", 1.0, torch.bfloat16)
+        ref[offsets[i]:offsets[i] + r * c].view(r, c).copy_(u)
+        ins.append(u.double().cpu().numpy())
+    out = ref.clone()
+    dm.ns_batched(shapes, ref, offsets, ws, ns_steps=5, variant=dm.NS_GRAM)
+    assert dm.stream_status(ws) == dm.OK
+    stream = torch.cuda.current_stream().cuda_stream
+    st = dm.lib().dmuon_ns_batched_noalloc(len(shapes), dm._shapes(shapes), out.data_ptr(),
+                                           dm._i64(offsets), 5, dm.NS_GRAM, None,
+                                           ctypes.c_float(1e-7), stream)
+    assert st == dm.OK, dm.status_string(st)
+    assert dm.noalloc_status() == dm.OK
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    for i, (r, c) in enumerate(shapes):
+        gram = dm.ns_variant_for((r, c), 5, dm.NS_GRAM) == dm.NS_GRAM
+        want = (oracle.gram_newton_schulz if gram else oracle.newton_schulz)(ins[i], 5)
+        got = out[offsets[i]:offsets[i] + r * c].view(r, c).double().cpu().numpy()
+        err = _rel(got, want)
+        assert err <= NS_TOL, f"{(r, c)} gram={gram}: rel err {err:.3e}"
