@@ -634,29 +634,66 @@ bool ns_standard(const GemmLauncher& L, const Request& R, const Plan& P, unsigne
 // Gram Newton-Schulz on buckets [b0, b1): A0 = X0 X0^T; per step
 // P = aI + bA + cA^2, Q = P Q, A' = A P^2; finally O = Q X0.  Slots: A in
 // SM0/SM1, P in SM2 (SM3 at step 0, where Q = P), Q in SM3/SM4, T = P^2 in SM5.
-bool ns_gram(const GemmLauncher& L, const Request& R) {
+// `before(i)`, when given, runs before the i-th product launch is enqueued
+// (the order of gram_launches below).
+bool ns_gram(const GemmLauncher& L, const Request& R,
+             const std::function<bool(int)>& before = nullptr) {
   const float a = R.abc[0], b = R.abc[1], c = R.abc[2];
+  int i = 0;
+  auto hook = [&]() { return !before || before(i++); };
   int sA = SM0, sAn = SM1, sQ = SM3, sQn = SM4;
-  if (!L.sym(SX0, SX0, SM0, sA, 0.f, 0.f, 1.f)) return false;
+  if (!hook() || !L.sym(SX0, SX0, SM0, sA, 0.f, 0.f, 1.f)) return false;
   for (int k = 0; k < R.ns_steps; ++k) {
     const bool last = k + 1 == R.ns_steps;
     const int sP = (k == 0) ? SM3 : SM2;
-    if (!L.sym(sA, sA, sA, sP, a, b, c)) return false;
+    if (!hook() || !L.sym(sA, sA, sA, sP, a, b, c)) return false;
     if (k > 0) {
-      if (!L.sym(sP, sQ, SM0, sQn, 0.f, 0.f, 1.f)) return false;
+      if (!hook() || !L.sym(sP, sQ, SM0, sQn, 0.f, 0.f, 1.f)) return false;
       std::swap(sQ, sQn);
     }
     if (!last) {
-      if (!L.sym(sP, sP, SM0, SM5, 0.f, 0.f, 1.f)) return false;
-      if (!L.sym(sA, SM5, SM0, sAn, 0.f, 0.f, 1.f)) return false;
+      if (!hook() || !L.sym(sP, sP, SM0, SM5, 0.f, 0.f, 1.f)) return false;
+      if (!hook() || !L.sym(sA, SM5, SM0, sAn, 0.f, 0.f, 1.f)) return false;
       std::swap(sA, sAn);
     }
   }
-  return L.full(sQ, SX0, SX0, SX0, 0.f, 1.f, true);
+  return hook() && L.full(sQ, SX0, SX0, SX0, 0.f, 1.f, true);
+}
+
+// The product launches of one Newton-Schulz run over a group of buckets, in
+// issue order, as the time model needs them: full (m x n output) or
+// symmetric (m x m), and whether the reduction runs over n (X X^T) or m.
+struct ProductLaunch {
+  bool full, k_is_n;
+};
+
+std::vector<ProductLaunch> standard_launches(int ns_steps) {
+  std::vector<ProductLaunch> v;
+  for (int k = 0; k < ns_steps; ++k) {
+    v.push_back({false, true});   // X X^T
+    v.push_back({false, false});  // A A
+    v.push_back({true, false});   // B X
+  }
+  return v;
+}
+
+std::vector<ProductLaunch> gram_launches(int ns_steps) {
+  std::vector<ProductLaunch> v;
+  v.push_back({false, true});     // X0 X0^T
+  for (int k = 0; k < ns_steps; ++k) {
+    v.push_back({false, false});  // P
+    if (k > 0) v.push_back({false, false});           // P Q
+    if (k + 1 < ns_steps) {
+      v.push_back({false, false});  // P P
+      v.push_back({false, false});  // A P^2
+    }
+  }
+  v.push_back({true, false});     // Q X0
+  return v;
 }
 
 // ------------------------------------------------------------------ step pipeline
-// The whole standard step runs its buckets in positions -- a position is a run
+// The whole step runs its buckets in positions -- a position is a run
 // of buckets (consecutive in the plan) whose products share launches -- and
 // overlaps its memory-bound work (momentum + pack, norm finish and relayout of
 // later positions; weight update of earlier ones) with the tensor-core
@@ -693,16 +730,16 @@ struct Piece {
 struct StepSchedule {
   std::vector<std::pair<int, int>> pos;               // bucket range [b0, b1) of each position
   std::vector<char> prepacked;                        // per position: packed on `s` first
-  std::vector<std::vector<Piece>> slot;               // [position * launches + i]: pieces next to it
+  std::vector<std::vector<std::vector<Piece>>> slot;  // [position][launch]: pieces next to it
   std::vector<Piece> tail_update;                     // update ranges run on `s` at the end
   double products = 0.0, exposed = 0.0;               // modelled seconds
 };
 
-// Modelled seconds of product phase i (= 3*step + {X X^T, A A, B X}) over the
-// buckets [b0, b1): one launch per run of buckets of one orientation, as the
-// launcher issues them.
-double model_phase_seconds(const Plan& P, int b0, int b1, int i, int clusters) {
-  const int phase = i % 3;
+// Modelled seconds of one product over the buckets [b0, b1): one launch per
+// run of buckets of one orientation, as the launcher issues them.
+double model_product_seconds(const Plan& P, int b0, int b1, const ProductLaunch& pl,
+                             int clusters) {
+  const int phase = pl.full ? 2 : 1;
   double total = 0.0;
   std::vector<double> load;
   int b = b0;
@@ -723,7 +760,7 @@ double model_phase_seconds(const Plan& P, int b0, int b1, int i, int clusters) {
         const BucketPlan& B = P.buckets[k];
         const long long n = (long long)B.mats.size() *
                             (phase == 2 ? (long long)B.full_ti * B.full_tj : (long long)B.sym.size());
-        const double K = phase == 0 ? double(B.n) : double(B.m);
+        const double K = pl.k_is_n ? double(B.n) : double(B.m);
         const double cost = 2.0 * kTileM * kTileN * K;
         const long long q = n / C, rem = n % C;
         for (int c = 0; c < C; ++c) load[size_t(c)] += double(q) * cost;
@@ -756,22 +793,25 @@ PieceCosts piece_costs(const Request& R) {
 StepSchedule plan_step(const Plan& P, const Request& R,
                        const std::vector<std::pair<int, int>>& pos, int clusters) {
   const int g = int(pos.size());
-  const int launches = 3 * R.ns_steps;
   const PieceCosts pc = piece_costs(R);
   StepSchedule S;
   S.pos = pos;
   S.prepacked.assign(size_t(g), 0);
   S.prepacked[0] = 1;
-  std::vector<double> dur(size_t(g) * size_t(launches));
+  std::vector<std::vector<double>> dur(static_cast<size_t>(g));
   S.products = 0.0;
-  for (int k = 0; k < g; ++k)
-    for (int i = 0; i < launches; ++i) {
-      dur[size_t(k) * size_t(launches) + size_t(i)] =
-          model_phase_seconds(P, pos[size_t(k)].first, pos[size_t(k)].second, i, clusters);
-      S.products += dur[size_t(k) * size_t(launches) + size_t(i)];
+  for (int k = 0; k < g; ++k) {
+    const int b0 = pos[size_t(k)].first, b1 = pos[size_t(k)].second;
+    const auto launches = P.buckets[b0].gram ? gram_launches(R.ns_steps)
+                                             : standard_launches(R.ns_steps);
+    for (const ProductLaunch& pl : launches) {
+      dur[size_t(k)].push_back(model_product_seconds(P, b0, b1, pl, clusters));
+      S.products += dur[size_t(k)].back();
     }
+  }
   for (;;) {
-    S.slot.assign(size_t(g) * size_t(launches), std::vector<Piece>());
+    S.slot.assign(size_t(g), std::vector<std::vector<Piece>>());
+    for (int k = 0; k < g; ++k) S.slot[size_t(k)].assign(dur[size_t(k)].size(), {});
     S.tail_update.clear();
     struct Todo { int pos, kind, bucket; long long lo, hi; };
     std::vector<Todo> mb, upd;
@@ -790,10 +830,10 @@ StepSchedule plan_step(const Plan& P, const Request& R,
     for (int k = 0; k < g && fail < 0; ++k) {
       // every later position's pack must be done before its products start
       if (mi < mb.size() && mb[mi].pos <= k) fail = mb[mi].pos;
-      for (int i = 0; i < launches && fail < 0; ++i) {
-        double budget = dur[size_t(k) * size_t(launches) + size_t(i)] * kModelCoBytes * kSlotFill;
+      for (size_t i = 0; i < dur[size_t(k)].size() && fail < 0; ++i) {
+        double budget = dur[size_t(k)][i] * kModelCoBytes * kSlotFill;
         if (budget < kMinPieceBytes) continue;
-        std::vector<Piece>& out = S.slot[size_t(k) * size_t(launches) + size_t(i)];
+        std::vector<Piece>& out = S.slot[size_t(k)][i];
         auto take = [&](Todo& t, double unit_bytes) {
           const long long can = unit_bytes > 0 ? (long long)(budget / unit_bytes) : t.hi - t.lo;
           const long long n = std::min(can, t.hi - t.lo);
@@ -841,9 +881,10 @@ StepSchedule plan_step(const Plan& P, const Request& R,
 // The candidate schedules of a whole step: one position per bucket, by size
 // (short first products, small up-front packs), the same with the second
 // position moved last (the last position's update is exposed), and one
-// position per orientation (wide/square buckets, tall buckets; fewer, fuller
-// launches for sets of small matrices).  The one with the least modelled
-// product plus exposed time runs.
+// position per run of buckets with the same form and orientation (fewer,
+// fuller launches for sets of small matrices).  The one with the least
+// modelled product plus exposed time runs.  A position never mixes the
+// standard and the Gram form.
 StepSchedule choose_step_schedule(const Plan& P, const Request& R, int clusters) {
   const int nb = int(P.buckets.size());
   std::vector<int> ord(static_cast<size_t>(nb));
@@ -862,13 +903,24 @@ StepSchedule choose_step_schedule(const Plan& P, const Request& R, int clusters)
     alt.push_back(second);
     cands.push_back(alt);
   }
-  int n_wide = 0;
-  while (n_wide < nb && !P.buckets[n_wide].tall) ++n_wide;
-  if (n_wide > 0 && n_wide < nb && nb > 2) {
-    long long cw = 0, ct = 0;
-    for (int b = 0; b < nb; ++b) (b < n_wide ? cw : ct) += P.buckets[b].chunks;
-    if (cw <= ct) cands.push_back({{0, n_wide}, {n_wide, nb}});
-    else cands.push_back({{n_wide, nb}, {0, n_wide}});
+  std::vector<std::pair<int, int>> runs;
+  for (int b = 0; b < nb;) {
+    int e = b + 1;
+    while (e < nb && P.buckets[e].tall == P.buckets[b].tall && P.buckets[e].gram == P.buckets[b].gram)
+      ++e;
+    runs.push_back({b, e});
+    b = e;
+  }
+  if (runs.size() >= 2 && int(runs.size()) < nb) {
+    auto chunks_of = [&](const std::pair<int, int>& r) {
+      long long c = 0;
+      for (int b = r.first; b < r.second; ++b) c += P.buckets[b].chunks;
+      return c;
+    };
+    std::stable_sort(runs.begin(), runs.end(), [&](const auto& x, const auto& y) {
+      return chunks_of(x) < chunks_of(y);
+    });
+    cands.push_back(runs);
   }
   StepSchedule best;
   bool have = false;
@@ -883,7 +935,7 @@ StepSchedule choose_step_schedule(const Plan& P, const Request& R, int clusters)
 }
 
 // Events used to order the two streams of an overlapped step; released when
-// the call returns (the driver keeps a pending event alive until it fires).
+// the call returns (the CUDA driver keeps a pending event alive until it fires).
 struct EventSet {
   std::vector<cudaEvent_t> e;
   bool create(int count) {
@@ -940,15 +992,15 @@ int run(const Request& R) {
 
   // A whole standard step over two or more buckets overlaps its memory-bound
   // work with the products (see choose_step_schedule and plan_step).
-  const bool overlap = R.do_pack && R.do_ns && R.do_update && R.ns_steps > 0 && P.n_std >= 2 &&
-                       P.n_std == nb && D.aux != nullptr;
+  const bool overlap = R.do_pack && R.do_ns && R.do_update && R.ns_steps > 0 && nb >= 2 &&
+                       D.aux != nullptr;
   if (overlap) {
     const StepSchedule S = choose_step_schedule(P, R, D.max_clusters);
     const int g = int(S.pos.size());
-    const int launches = 3 * R.ns_steps;
     cudaStream_t x = aux_stream_for(D, s);
     size_t n_slots = 0;
-    for (const auto& v : S.slot) n_slots += v.empty() ? 0 : 1;
+    for (const auto& v : S.slot)
+      for (const auto& w : v) n_slots += w.empty() ? 0 : 1;
     EventSet ev;  // [0, g): position k's pack done on aux; g: aux done; then one per used slot
     if (!ev.create(g + 1 + int(n_slots))) return DMUON_ERR_CUDA;
     size_t next_ev = size_t(g) + 1;
@@ -997,7 +1049,7 @@ int run(const Request& R) {
       if (!S.prepacked[size_t(k)] && cudaStreamWaitEvent(s, ev.e[size_t(k)], 0) != cudaSuccess)
         return DMUON_ERR_CUDA;
       auto before = [&](int i) {
-        const auto& pieces = S.slot[size_t(k) * size_t(launches) + size_t(i)];
+        const auto& pieces = S.slot[size_t(k)][size_t(i)];
         if (pieces.empty()) return true;
         // the pieces start together with this product launch
         cudaEvent_t e = ev.e[next_ev++];
@@ -1007,9 +1059,10 @@ int run(const Request& R) {
           if (!run_piece(pc)) return false;
         return true;
       };
-      if (!ns_standard(GemmLauncher(P, R, D.max_clusters, ws, S.pos[size_t(k)].first,
-                                    S.pos[size_t(k)].second, s),
-                       R, P, ws, before))
+      const GemmLauncher L(P, R, D.max_clusters, ws, S.pos[size_t(k)].first,
+                           S.pos[size_t(k)].second, s);
+      if (!(P.buckets[S.pos[size_t(k)].first].gram ? ns_gram(L, R, before)
+                                                   : ns_standard(L, R, P, ws, before)))
         return DMUON_ERR_CUDA;
     }
     for (const Piece& t : S.tail_update) {

@@ -61,14 +61,19 @@ def test_resume_from_saved_state_is_bit_identical(dm):
     assert not _same(W3, W2)          # the third step did change the weights
 
 
-def test_overlapped_step_equals_three_separate_calls(dm):
-    """dmuon_muon_step runs the memory-bound kernels of one bucket group on a
-    second stream next to the other group's products; the result must be the
-    same bits as pack, Newton-Schulz and update called one after another."""
+@pytest.mark.parametrize("variant", [0, 1])
+def test_overlapped_step_equals_three_separate_calls(dm, variant):
+    """dmuon_muon_step runs the memory-bound kernels of later and earlier buckets
+    on a second stream next to the current bucket's products, bucket by bucket;
+    the result must be the same bits as pack, Newton-Schulz and update called one
+    after another over all buckets -- with the standard form and with the Gram
+    variant (whose rule gives the rectangular matrices here the Gram form)."""
     from newton_schulz_owner_gb300 import workloads as wl
+    if variant == 1:
+        assert any(dm.ns_variant_for(s, 5, dm.NS_GRAM) == dm.NS_GRAM for s in SHAPES)
     outs = []
     for mode in ("whole", "three"):
-        own = dm.MuonOwner(SHAPES)
+        own = dm.MuonOwner(SHAPES, variant=variant)
         W = [wl.random_matrix(s, 700 + i, "cuda", 0.02, torch.bfloat16) for i, s in enumerate(SHAPES)]
         M = [torch.zeros(s, device="cuda") for s in SHAPES]
         for k in range(2):
@@ -79,7 +84,7 @@ def test_overlapped_step_equals_three_separate_calls(dm):
             else:
                 dm.pack(SHAPES, G, M, 0.95, own.packed, own.offsets, own.workspace)
                 dm.ns_batched(SHAPES, own.packed, own.offsets, own.workspace, ns_steps=5,
-                              use_pack_norms=True)
+                              variant=variant, use_pack_norms=True)
                 dm.unpack_update(SHAPES, W, 0.02, own.packed, own.offsets, own.workspace)
             assert own.status() == dm.OK
         torch.cuda.synchronize()
