@@ -880,9 +880,10 @@ StepSchedule plan_step(const Plan& P, const Request& R,
 
 // The candidate schedules of a whole step: one position per bucket, by size
 // (short first products, small up-front packs), the same with the second
-// position moved last (the last position's update is exposed), and one
-// position per run of buckets with the same form and orientation (fewer,
-// fuller launches for sets of small matrices).  The one with the least
+// position moved last (the last position's update is exposed), buckets too
+// small to occupy every CTA pair joined with a neighbour, and one position per
+// run of buckets with the same form and orientation (fewer, fuller launches for
+// sets of small matrices).  The one with the least
 // modelled product plus exposed time runs.  A position never mixes the
 // standard and the Gram form.
 StepSchedule choose_step_schedule(const Plan& P, const Request& R, int clusters) {
@@ -903,6 +904,41 @@ StepSchedule choose_step_schedule(const Plan& P, const Request& R, int clusters)
     alt.push_back(second);
     cands.push_back(alt);
   }
+  auto chunks_of = [&](const std::pair<int, int>& r) {
+    long long c = 0;
+    for (int b = r.first; b < r.second; ++b) c += P.buckets[b].chunks;
+    return c;
+  };
+  auto by_size = [&](std::vector<std::pair<int, int>>& v) {
+    std::stable_sort(v.begin(), v.end(), [&](const auto& x, const auto& y) {
+      return chunks_of(x) < chunks_of(y);
+    });
+  };
+  // buckets whose symmetric products cannot occupy every CTA pair (fewer tiles
+  // than pairs) joined with their neighbour of the same form and orientation
+  {
+    auto small = [&](int b) {
+      return (long long)P.buckets[b].mats.size() * (long long)P.buckets[b].sym.size() < clusters;
+    };
+    auto same = [&](int x, int y) {
+      return P.buckets[x].tall == P.buckets[y].tall && P.buckets[x].gram == P.buckets[y].gram;
+    };
+    std::vector<std::pair<int, int>> merged;
+    for (int b = 0; b < nb; ++b) {
+      // a small bucket joins the position before it when that one is of the
+      // same kind (and only one bucket long, or small itself), else starts one
+      if (!merged.empty() && same(merged.back().first, b) && merged.back().second == b &&
+          (small(b) || (merged.back().second - merged.back().first == 1 &&
+                        small(merged.back().first))))
+        merged.back().second = b + 1;
+      else
+        merged.push_back({b, b + 1});
+    }
+    if (int(merged.size()) < nb && merged.size() >= 2) {
+      by_size(merged);
+      cands.push_back(merged);
+    }
+  }
   std::vector<std::pair<int, int>> runs;
   for (int b = 0; b < nb;) {
     int e = b + 1;
@@ -912,14 +948,7 @@ StepSchedule choose_step_schedule(const Plan& P, const Request& R, int clusters)
     b = e;
   }
   if (runs.size() >= 2 && int(runs.size()) < nb) {
-    auto chunks_of = [&](const std::pair<int, int>& r) {
-      long long c = 0;
-      for (int b = r.first; b < r.second; ++b) c += P.buckets[b].chunks;
-      return c;
-    };
-    std::stable_sort(runs.begin(), runs.end(), [&](const auto& x, const auto& y) {
-      return chunks_of(x) < chunks_of(y);
-    });
+    by_size(runs);
     cands.push_back(runs);
   }
   StepSchedule best;
