@@ -189,14 +189,15 @@ int dmuon_unpack_update(int n, const dmuon_shape* shp, void* const* weight,
  * dmuon_muon_step -- the whole owner-side Muon step: dmuon_pack, then
  * dmuon_ns_batched(use_pack_norms = 1) with the default coefficients and
  * eps = 1e-7, then dmuon_unpack_update, enqueued on `stream`.
- * With the standard variant, ns_steps >= 1 and two or more distinct working
- * shapes (or orientations), the step overlaps its memory-bound kernels with
- * the tensor-core products: it visits the shape groups in order of size, and
- * while one group is orthogonalised, later groups are packed and relaid out
- * and earlier groups' weights are updated, in pieces that each start together
- * with one long product launch and are sized (by a time model) to finish
- * inside it; what does not fit -- the packs of the first groups, the last
- * group's update -- runs alone on `stream`.  The overlapped work runs on a
+ * With ns_steps >= 1 and two or more distinct working shapes (or
+ * orientations, or forms under the Gram variant), the step overlaps its
+ * memory-bound kernels with the tensor-core products: it visits groups of
+ * shapes in turn (an order and grouping a time model of the launches picks),
+ * and while one group is orthogonalised, later groups are packed and relaid
+ * out and earlier groups' weights are updated, in pieces that each start
+ * together with one long product launch and are sized to finish inside it;
+ * what does not fit -- the packs of the first groups, the last group's update
+ * -- runs alone on `stream`.  The overlapped work runs on a
  * lowest-priority companion stream that the library creates for `stream` on
  * its first call with it (one per caller stream, up to 16 per device; past
  * that, and while `stream` is being captured, a companion shared by the device

@@ -426,6 +426,26 @@ def test_two_owners_on_two_streams_run_concurrently_and_match(dm, wl):
             assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
+@pytest.mark.parametrize("ns_steps", [1, 2, 8])
+def test_muon_step_other_step_counts(dm, wl, ns_steps):
+    """The pipelined step places its memory-bound pieces by product launch, and
+    the launches per bucket follow the step count: a ragged multi-bucket step
+    at 1, 2 and 8 Newton-Schulz steps, against the oracle."""
+    shapes = [(256, 700), (700, 256), (300, 900), (900, 300), (256, 256), (64, 1000)]
+    _muon_case(dm, wl, shapes, torch.bfloat16, torch.float32, steps=1, seed=29,
+               ns_steps=ns_steps)
+
+
+@pytest.mark.parametrize("ns_steps", [3, 8])
+def test_muon_step_gram_variant_other_step_counts(dm, wl, ns_steps):
+    """The Gram form's positions in the pipelined step (their launch count
+    depends on the step count), next to standard ones."""
+    shapes = [(256, 256), (64, 256), (700, 256), (256, 700), (300, 900)]
+    assert any(dm.ns_variant_for(s, ns_steps, dm.NS_GRAM) == dm.NS_GRAM for s in shapes)
+    _muon_case(dm, wl, shapes, torch.bfloat16, torch.float32, steps=1, variant=1, seed=31,
+               ns_steps=ns_steps)
+
+
 def test_muon_step_gram_variant(dm, wl):
     shapes = [(256, 256), (64, 256), (700, 256), (256, 700)]
     _muon_case(dm, wl, shapes, torch.bfloat16, torch.float32, variant=1)
