@@ -253,6 +253,26 @@ def trace_summary(rec, step_ms: float):
                     "the time outside MMA-active"}
 
 
+def e2e_group_bounds(layers: int, groups: int, taper: bool):
+    """Layer ranges of the end-to-end loop's groups.  Only the first group's copy
+    in and the last group's copy out are not hidden behind another group's
+    compute, so with `taper` the groups grow towards the middle (weights
+    1, 2, 4, ..., 4, 2, 1) and those two stay small; otherwise equal groups."""
+    groups = max(1, min(groups, layers))
+    if taper and groups >= 3:
+        half = [2 ** min(k, 2) for k in range((groups + 1) // 2)]
+        wts = half + half[:groups // 2][::-1]
+    else:
+        wts = [1] * groups
+    tot = float(sum(wts))
+    cuts, acc = [0], 0.0
+    for wgt in wts[:-1]:
+        acc += wgt
+        cuts.append(max(cuts[-1] + 1, min(layers - (len(wts) - len(cuts)), round(layers * acc / tot))))
+    cuts.append(layers)
+    return [(cuts[k], cuts[k + 1]) for k in range(len(wts)) if cuts[k] < cuts[k + 1]]
+
+
 def owner_times(dmuon, shapes, owner, variant, ns_steps, stream, barrier, grouped_ns_ms):
     """Each LPT owner's Newton-Schulz as its own call on its segments of the
     packed buffer, back to back, against all owners in one grouped call: the
@@ -628,9 +648,9 @@ def run_gpu(args, rank, world, local_rank):
         d2h_stream = torch.cuda.Stream(device=dev)
         # groups of whole layers, each a contiguous range of every flat buffer
         per_layer = max(1, n // max(1, w.layers))
-        n_groups = max(1, min(args.e2e_groups, n // per_layer))
-        bounds = [round(g_ * (n // per_layer) / n_groups) * per_layer for g_ in range(n_groups)] + [n]
-        gsets = [(bounds[j], bounds[j + 1]) for j in range(n_groups) if bounds[j] < bounds[j + 1]]
+        gsets = [(a * per_layer, min(n, b * per_layer))
+                 for a, b in e2e_group_bounds(n // per_layer, args.e2e_groups, args.e2e_taper)]
+        gsets[-1] = (gsets[-1][0], n)
         owner = None   # the groups' owners take its place
         torch.cuda.empty_cache()
         g_owner = [dmuon.MuonOwner(shapes[i0:i1], n_owners=w.n_owners, variant=args.variant,
@@ -813,6 +833,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-groups", type=int, default=4,
                     help="layer groups of the end-to-end loop (one dmuon_muon_step call each)")
+    ap.add_argument("--e2e-taper", type=int, default=0,
+                    help="1: end-to-end groups grow towards the middle (small first and last "
+                         "groups, whose copies are not hidden)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-launch-count", action="store_true",
                     help="accepted for older command lines; the launch count now comes "

@@ -97,3 +97,18 @@ def test_bench_flop_counts_agree_with_the_oracle(steps):
     assert b.ns_flops(shapes, steps) == pytest.approx(oracle.ns_flops_algorithmic(shapes, steps))
     assert b.gram_flops(shapes, steps) == pytest.approx(
         oracle.gram_ns_flops_algorithmic(shapes, steps))
+
+
+@pytest.mark.parametrize("layers", [1, 3, 28, 32])
+@pytest.mark.parametrize("groups", [1, 2, 4, 6, 8])
+@pytest.mark.parametrize("taper", [False, True])
+def test_e2e_groups_cover_every_layer_once(layers, groups, taper):
+    b = _bench()
+    g = b.e2e_group_bounds(layers, groups, taper)
+    assert g[0][0] == 0 and g[-1][1] == layers
+    assert all(lo < hi for lo, hi in g)
+    assert all(g[k][1] == g[k + 1][0] for k in range(len(g) - 1))
+    assert len(g) <= max(1, min(groups, layers))
+    if taper and layers >= 16 and groups >= 4:
+        sizes = [hi - lo for lo, hi in g]
+        assert sizes[0] < max(sizes) and sizes[-1] < max(sizes)

@@ -426,11 +426,13 @@ def test_two_owners_on_two_streams_run_concurrently_and_match(dm, wl):
             assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
-@pytest.mark.parametrize("ns_steps", [1, 2, 8])
+@pytest.mark.parametrize("ns_steps", [0, 1, 2, 8])
 def test_muon_step_other_step_counts(dm, wl, ns_steps):
     """The pipelined step places its memory-bound pieces by product launch, and
     the launches per bucket follow the step count: a ragged multi-bucket step
-    at 1, 2 and 8 Newton-Schulz steps, against the oracle."""
+    at 1, 2 and 8 Newton-Schulz steps, against the oracle; and at 0 steps (no
+    products: O is the normalised U, and the step runs its three parts in
+    turn)."""
     shapes = [(256, 700), (700, 256), (300, 900), (900, 300), (256, 256), (64, 1000)]
     _muon_case(dm, wl, shapes, torch.bfloat16, torch.float32, steps=1, seed=29,
                ns_steps=ns_steps)
