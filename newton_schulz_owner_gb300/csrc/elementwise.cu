@@ -352,11 +352,14 @@ DM_DEV void store8f(float* base, long long e, const float (&f)[8]) {
 // AdamW with decoupled weight decay, fp32 arithmetic:
 //   p <- p * decay;  m <- b1 m + (1-b1) g;  v <- b2 v + (1-b2) g^2;
 //   p <- p - step_size * m / (sqrt(v) * inv_bc2_sqrt + eps)
+// At most 64 registers where that needs no spills (bf16 parameter or
+// gradient), so that four blocks fit on an SM: with seven streams per element
+// the kernel needs many loads in flight to cover DRAM latency.
 template <bool P_BF16, bool G_BF16>
-__global__ void __launch_bounds__(kEwThreads) adamw_kernel(const AdamTensor* __restrict__ ts,
-                                                           int n, AdamScalars ks) {
+__global__ void __launch_bounds__(kEwThreads, (P_BF16 || G_BF16) ? 4 : 3)
+    adamw_kernel(const AdamTensor* __restrict__ ts, int n, AdamScalars ks) {
   const long long chunk = blockIdx.x;
-  const AdamTensor& T = ts[find_adam(ts, n, chunk)];
+  const AdamTensor T = ts[find_adam(ts, n, chunk)];
   const long long start = (chunk - T.chunk_begin) * kChunk;
   const long long end = min(T.numel, start + kChunk);
   const float b1 = ks.b1, b2 = ks.b2, omb1 = ks.omb1, omb2 = ks.omb2;
