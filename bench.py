@@ -139,6 +139,14 @@ def ns_flops(shapes, ns_steps: int) -> float:
                      for s in shapes))
 
 
+def nominal_flops(shapes, ns_steps: int) -> float:
+    """Nominal dense flops of the standard iteration, every product counted in
+    full (X X^T 2 m^2 n, A A 2 m^3, B X 2 m^2 n): the count a dense GEMM library
+    would report for the same products."""
+    return float(sum((4.0 * min(s) ** 2 * max(s) + 2.0 * float(min(s)) ** 3) * ns_steps
+                     for s in shapes))
+
+
 def gram_flops(shapes, ns_steps: int) -> float:
     """Algorithmic flops of the Gram iteration: A0 = X0 X0^T (m^2 n, half) and
     O = Q X0 (2 m^2 n), and per step the symmetric m^3 products A A, P Q (not
@@ -384,6 +392,8 @@ def config_point(dmuon, wl, name, variant, ns_steps, dev, gpu_index, peak, steps
            "pack_ms": statistics.median(p[0].elapsed_time(p[1]) for p in ph),
            "update_ms": statistics.median(p[2].elapsed_time(p[3]) for p in ph),
            "ns_tflops_algorithmic": flops / (ns_ms * 1e-3) / 1e12,
+           "ns_tflops_nominal_dense": None if gs else
+           nominal_flops(shapes, ns_steps) / (ns_ms * 1e-3) / 1e12,
            "ns_frac_of_peak": flops / (ns_ms * 1e-3) / 1e12 / peak,
            "matrices_per_s": len(shapes) / (step_ms * 1e-3), "steps": steps, "warmup": warmup,
            "clocks": clocks}
@@ -478,6 +488,8 @@ def run_gpu(args, rank, world, local_rank):
     gs = [s for s in shapes if dmuon.ns_variant_for(s, args.ns_steps, args.variant) == 1]
     ss = [s for s in shapes if dmuon.ns_variant_for(s, args.ns_steps, args.variant) != 1]
     flops = gram_flops(gs, args.ns_steps) + ns_flops(ss, args.ns_steps)
+    # nominal dense count (standard form only): both symmetric products counted in full
+    flops_nominal = nominal_flops(shapes, args.ns_steps) if not gs else None
     elems = sum(r * c for r, c in shapes)
 
     def step_phases(ev=None):
@@ -789,6 +801,8 @@ def run_gpu(args, rank, world, local_rank):
                    "l2": f"no flush: resident inputs {resident / 1e9:.1f} GB >> L2 "
                          f"{L2_BYTES / 2**20:.0f} MB"},
         "ns_tflops": achieved_tflops,
+        "ns_tflops_nominal_dense": None if flops_nominal is None else
+        flops_nominal / (ns_mean * 1e-3) / 1e12,
         "matrices_per_s": n * world / (ms * 1e-3),
         "phases": phases,
         "roofline": roofline,

@@ -112,3 +112,11 @@ def test_e2e_groups_cover_every_layer_once(layers, groups, taper):
     if taper and layers >= 16 and groups >= 4:
         sizes = [hi - lo for lo, hi in g]
         assert sizes[0] < max(sizes) and sizes[-1] < max(sizes)
+
+
+def test_nominal_flops_count_every_product_in_full():
+    b = _bench()
+    s = [(1024, 4096)]
+    m, n = 1024, 4096
+    assert b.nominal_flops(s, 5) == pytest.approx(5 * (2 * m * m * n + 2 * m ** 3 + 2 * m * m * n))
+    assert b.nominal_flops(s, 5) > b.ns_flops(s, 5)
