@@ -85,16 +85,39 @@ struct Kind {
   static constexpr bool swap_lr = KIND == kFullTall;
 };
 
+// Each role walks its tiles in increasing order, so the bucket of the next
+// tile is found by moving a cursor forward (a load per bucket boundary)
+// instead of a search per tile.  The MMA thread needs only the K extent of the
+// bucket, which it takes from the cursor without touching the tile tables:
+// that thread issues the tensor-core work, and any latency in its loop leaves
+// the tensor pipe idle.
 template <int KIND>
-DM_DEV TileInfo decode_tile(const GemmArgs& g, int t) {
-  constexpr bool FULL = Kind<KIND>::full;
-  int lo = 0, hi = g.n_buckets - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    const int b = FULL ? g.buckets[mid].full_begin : g.buckets[mid].sym_begin;
-    if (b <= t) lo = mid;
-    else hi = mid - 1;
+struct BucketCursor {
+  int b = 0;
+  int next = 0x7fffffff;  // first tile of bucket b + 1
+  DM_DEV static int begin(const GemmArgs& g, int k) {
+    return Kind<KIND>::full ? g.buckets[k].full_begin : g.buckets[k].sym_begin;
   }
+  DM_DEV void init(const GemmArgs& g) {
+    b = 0;
+    next = g.n_buckets > 1 ? begin(g, 1) : 0x7fffffff;
+  }
+  // move to the bucket holding tile t (t never decreases); true if it moved
+  DM_DEV bool seek(const GemmArgs& g, int t) {
+    bool moved = false;
+    while (t >= next) {
+      ++b;
+      next = b + 1 < g.n_buckets ? begin(g, b + 1) : 0x7fffffff;
+      moved = true;
+    }
+    return moved;
+  }
+};
+
+// Tile t of bucket `lo`: matrix and tile coordinates.
+template <int KIND>
+DM_DEV TileInfo decode_tile(const GemmArgs& g, int lo, int t) {
+  constexpr bool FULL = Kind<KIND>::full;
   const Bucket& B = g.buckets[lo];
   TileInfo T;
   T.bucket = lo;
@@ -152,16 +175,19 @@ DM_DEV void producer(const GemmArgs& g, uint32_t rank, uint8_t* sA, uint8_t* sB,
   const int clusters = int(cluster_count_x());
   int stage = 0;
   uint32_t phase = 0;
-  int prev_bucket = -1;
+  BucketCursor<KIND> cur;
+  cur.init(g);
+  bool first = true;
   for (int t = int(cluster_id_x()); t < g.total_tiles; t += clusters) {
-    const TileInfo T = decode_tile<KIND>(g, g.tile_base + t);
+    const bool moved = cur.seek(g, g.tile_base + t);
+    const TileInfo T = decode_tile<KIND>(g, cur.b, g.tile_base + t);
     const Bucket& B = g.buckets[T.bucket];
     const void* mapL = tmap_of(g, B, Kind<KIND>::swap_lr ? g.sR : g.sL);
     const void* mapR = tmap_of(g, B, Kind<KIND>::swap_lr ? g.sL : g.sR);
-    if (T.bucket != prev_bucket) {
+    if (moved || first) {
       tensormap_acquire(mapL);
       tensormap_acquire(mapR);
-      prev_bucket = T.bucket;
+      first = false;
     }
     const int KB = (k_extent<KIND>(g, B) + kBK - 1) / kBK;
     const int row0 = T.ti * kTileM + int(rank) * kCtaM;        // this CTA's rows of L
@@ -209,7 +235,7 @@ DM_DEV void producer(const GemmArgs& g, uint32_t rank, uint8_t* sA, uint8_t* sB,
   }
 }
 
-template <int KIND>
+template <int KIND, bool TRACE>
 DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* full_bar,
                        uint64_t* empty_bar, uint64_t* tfull, uint64_t* tempty,
                        uint64_t* drain_bar, uint32_t tmem_base, volatile int* abort_flag,
@@ -217,16 +243,17 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
   constexpr uint32_t idesc = idesc_bf16(kTileM, kTileN, Kind<KIND>::l_mn, Kind<KIND>::r_mn);
   const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
   const int clusters = int(cluster_count_x());
-  const bool tracing = g.trace != nullptr;
+  constexpr bool tracing = TRACE;
   long long wait_op = 0, wait_acc = 0;
   const long long c_first = tracing ? clock64() : 0;
   int stage = 0;
   uint32_t phase = 0;
   int it = 0;
+  BucketCursor<KIND> cur;
+  cur.init(g);
+  int KB = (k_extent<KIND>(g, g.buckets[0]) + kBK - 1) / kBK;
   for (int t = int(cluster_id_x()); t < g.total_tiles; t += clusters, ++it) {
-    const TileInfo T = decode_tile<KIND>(g, g.tile_base + t);
-    const Bucket& B = g.buckets[T.bucket];
-    const int KB = (k_extent<KIND>(g, B) + kBK - 1) / kBK;
+    if (cur.seek(g, g.tile_base + t)) KB = (k_extent<KIND>(g, g.buckets[cur.b]) + kBK - 1) / kBK;
     // Descriptors of stage 0, K-step 0; the start-address field (bits 0-13,
     // address >> 4) then advances by a constant per stage and per K-step of
     // 16 elements: K-major 32 bytes along the swizzled 128-byte row (8-row
@@ -412,8 +439,12 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
   };
 
   int t = int(cluster_id_x());
+  BucketCursor<KIND> cur;
+  cur.init(g);
   if (aux_tma && t < g.total_tiles && lane == 0) {
-    const TileInfo T = decode_tile<KIND>(g, g.tile_base + t);
+    BucketCursor<KIND> c0 = cur;
+    c0.seek(g, g.tile_base + t);
+    const TileInfo T = decode_tile<KIND>(g, c0.b, g.tile_base + t);
     const Bucket& B = g.buckets[T.bucket];
     acquire_maps(T.bucket, B);
     issue_aux(T, B, 0);
@@ -427,7 +458,8 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
   const bool sym_aux = !FULL && g.beta != 0.f;
   uint4 a_cur[4];
   for (; ok && t < g.total_tiles; t += clusters, ++it) {
-    const TileInfo T = decode_tile<KIND>(g, g.tile_base + t);
+    cur.seek(g, g.tile_base + t);
+    const TileInfo T = decode_tile<KIND>(g, cur.b, g.tile_base + t);
     const Bucket& B = g.buckets[T.bucket];
     if (lane == 0) acquire_maps(T.bucket, B);
     const int acc = it & 1;
@@ -569,7 +601,9 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
     if (lane == 0) mbar_arrive_cluster(leader_tempty + uint32_t(acc) * 8u);
     // operands of the next tile's first two chunks
     if (ok && aux_tma && lane == 0 && t + clusters < g.total_tiles) {
-      const TileInfo Tn = decode_tile<KIND>(g, g.tile_base + t + clusters);
+      BucketCursor<KIND> cn = cur;
+      cn.seek(g, g.tile_base + t + clusters);
+      const TileInfo Tn = decode_tile<KIND>(g, cn.b, g.tile_base + t + clusters);
       const Bucket& Bn = g.buckets[Tn.bucket];
       acquire_maps(Tn.bucket, Bn);
       if (!g.final_out) bulk_wait_read<0>();
@@ -582,7 +616,10 @@ DM_DEV void epilogue(const GemmArgs& g, uint32_t rank, uint64_t* tfull, uint64_t
   __syncwarp();
 }
 
-template <int KIND>
+// TRACE: the instance for traced launches (dmuon_trace_begin), which stamps
+// times and counts the MMA thread's waits; the untraced instance carries none
+// of that code.
+template <int KIND, bool TRACE>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -600,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // first / last MMA time and the MMA thread's wait cycles (traced launches only)
   unsigned long long* tstamp = reinterpret_cast<unsigned long long*>(aux_bar + 2 * kEpiWarps + 1);
-  const unsigned long long t_entry = g.trace != nullptr ? globaltimer_ns() : 0ull;
+  const unsigned long long t_entry = TRACE ? globaltimer_ns() : 0ull;
 
   const int warp = threadIdx.x >> 5;
   const uint32_t rank = cluster_rank();
@@ -632,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     producer<KIND>(g, rank, sA, sB, full_bar, empty_bar, abort_flag);
   } else if (threadIdx.x == 32) {
     if (rank == 0)
-      mma_issuer<KIND>(g, sA, sB, full_bar, empty_bar, tfull, tempty, drain_bar, tmem_base,
+      mma_issuer<KIND, TRACE>(g, sA, sB, full_bar, empty_bar, tfull, tempty, drain_bar, tmem_base,
                        abort_flag, tstamp);
   } else if (warp >= 2) {
     epilogue<KIND>(g, rank, tfull, tempty, aux_bar, smem_u32(sE), tmem_base, abort_flag);
@@ -650,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, kTmemCols);
   }
-  if (g.trace != nullptr && threadIdx.x == 0) {
+  if (TRACE && threadIdx.x == 0) {
     TraceRec r;
     r.launch = g.trace_launch;
     r.cta = blockIdx.x;
@@ -728,19 +765,24 @@ cudaError_t launch_diag_shift(const Bucket* buckets, int n_buckets, int first_in
 
 size_t ns_gemm_smem_bytes() { return kSmemBytes; }
 
-template <int KIND>
-cudaError_t prepare_kind(int num_sms, int* max_clusters) {
-  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<KIND>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+cudaError_t prepare_instance(void (*kernel)(GemmArgs), int num_sms, int* max_clusters) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(kSmemBytes));
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg = pair_config(num_sms / 2, nullptr, &attr);
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, ns_gemm_kernel<KIND>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
   if (e != cudaSuccess) return e;
   if (n < *max_clusters) *max_clusters = n;
   return cudaSuccess;
+}
+
+template <int KIND>
+cudaError_t prepare_kind(int num_sms, int* max_clusters) {
+  cudaError_t e = prepare_instance(ns_gemm_kernel<KIND, false>, num_sms, max_clusters);
+  if (e == cudaSuccess) e = prepare_instance(ns_gemm_kernel<KIND, true>, num_sms, max_clusters);
+  return e;
 }
 
 cudaError_t ns_gemm_prepare(int num_sms, int* max_clusters) {
@@ -797,12 +839,22 @@ cudaError_t launch_ns_gemm(const GemmArgs& g_in, int kind, int max_clusters, cud
   }
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg = pair_config(clusters, s, &attr);
+  const bool tr = g.trace != nullptr;
   switch (kind) {
-    case kSymK: return counted(cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kSymK>, g));
-    case kSymMN: return counted(cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kSymMN>, g));
-    case kFullWide: return counted(cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kFullWide>, g));
-    case kFullTall: return counted(cudaLaunchKernelEx(&cfg, ns_gemm_kernel<kFullTall>, g));
-    default: return cudaErrorInvalidValue;
+    case kSymK:
+      return counted(cudaLaunchKernelEx(
+          &cfg, tr ? ns_gemm_kernel<kSymK, true> : ns_gemm_kernel<kSymK, false>, g));
+    case kSymMN:
+      return counted(cudaLaunchKernelEx(
+          &cfg, tr ? ns_gemm_kernel<kSymMN, true> : ns_gemm_kernel<kSymMN, false>, g));
+    case kFullWide:
+      return counted(cudaLaunchKernelEx(
+          &cfg, tr ? ns_gemm_kernel<kFullWide, true> : ns_gemm_kernel<kFullWide, false>, g));
+    case kFullTall:
+      return counted(cudaLaunchKernelEx(
+          &cfg, tr ? ns_gemm_kernel<kFullTall, true> : ns_gemm_kernel<kFullTall, false>, g));
+    default:
+      return cudaErrorInvalidValue;
   }
 }
 
