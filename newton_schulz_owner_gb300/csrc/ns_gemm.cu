@@ -19,9 +19,9 @@
 //
 // Work unit: a 256 x 256 output tile computed by a cluster of two CTAs on two
 // SMs with one tcgen05.mma.cta_group::2 (M=256, N=256, K=16).  Each CTA loads
-// only its 128 rows of L and its 128 columns of R per 64-wide K block (32 KB),
+// only its 128 rows of L and its 128 columns of R per 128-wide K block (64 KB),
 // half of what a single SM needs for a 128 x 256 tile at the same tensor
-// rate, which leaves room for a 6-stage ring in 192 KB of shared memory.
+// rate, which leaves room for a 3-stage ring in 192 KB of shared memory.
 //
 // CTA layout (320 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (both CTAs): completion counted on the leader's
@@ -47,9 +47,16 @@
 namespace dm {
 namespace {
 
-constexpr int kStages = 6;
-constexpr int kAStage = kCtaM * kBK * 2;         // 16 KB: this CTA's 128 rows of L
-constexpr int kBStage = (kTileN / 2) * kBK * 2;  // 16 KB: this CTA's 128 columns of R
+// Three stages of 128 K-elements: the same bytes in flight as six of 64, with
+// half the barrier round trips and commits per MMA.  Measured on Llama-3.1-8B:
+// 1% faster and about 3.5% higher SM clock under the power cap.
+constexpr int kStages = 3;
+constexpr int kAStage = kCtaM * kBK * 2;         // 32 KB: this CTA's 128 rows of L
+constexpr int kBStage = (kTileN / 2) * kBK * 2;  // 32 KB: this CTA's 128 columns of R
+// A stage holds kPanels panels of 64 K-elements (the span of one 128-byte
+// swizzled row); each panel is two TMA boxes of 64 rows.
+constexpr int kPanels = kBK / 64;
+constexpr int kAPanel = kAStage / kPanels, kBPanel = kBStage / kPanels;
 constexpr int kStageBytes = kAStage + kBStage;
 constexpr int kPairTxBytes = 2 * kStageBytes;    // both CTAs' loads land on the leader's barrier
 constexpr int kBox = 64 * 64 * 2;                // one TMA box: 64 rows x 128 bytes
@@ -209,23 +216,27 @@ DM_DEV void producer(const GemmArgs& g, uint32_t rank, uint8_t* sA, uint8_t* sB,
         return;
       }
       if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], kPairTxBytes);
-      uint8_t* a = sA + stage * kAStage;
-      uint8_t* b = sB + stage * kBStage;
       const uint32_t bar = leader_full + uint32_t(stage) * 8u;
-      const int k0 = (k_reverse ? KB - 1 - kb : kb) * kBK;
-      if (Kind<KIND>::l_mn) {  // 64 K-rows x 64 rows of L per box
-        tma_load_3d_pair(a, mapL, bar, row0, k0, T.mat);
-        tma_load_3d_pair(a + kBox, mapL, bar, row0 + 64, k0, T.mat);
-      } else {        // 64 rows of L x 64 K-elements per box
-        tma_load_3d_pair(a, mapL, bar, k0, row0, T.mat);
-        tma_load_3d_pair(a + kBox, mapL, bar, k0, row0 + 64, T.mat);
-      }
-      if (Kind<KIND>::r_mn) {
-        tma_load_3d_pair(b, mapR, bar, col0, k0, T.mat);
-        tma_load_3d_pair(b + kBox, mapR, bar, col0 + 64, k0, T.mat);
-      } else {
-        tma_load_3d_pair(b, mapR, bar, k0, col0, T.mat);
-        tma_load_3d_pair(b + kBox, mapR, bar, k0, col0 + 64, T.mat);
+      // K past the end (a last stage that is only partly inside) reads as zeros
+#pragma unroll
+      for (int pp = 0; pp < kPanels; ++pp) {
+        uint8_t* a = sA + stage * kAStage + pp * kAPanel;
+        uint8_t* b = sB + stage * kBStage + pp * kBPanel;
+        const int k0 = (k_reverse ? KB - 1 - kb : kb) * kBK + pp * 64;
+        if (Kind<KIND>::l_mn) {  // 64 K-rows x 64 rows of L per box
+          tma_load_3d_pair(a, mapL, bar, row0, k0, T.mat);
+          tma_load_3d_pair(a + kBox, mapL, bar, row0 + 64, k0, T.mat);
+        } else {        // 64 rows of L x 64 K-elements per box
+          tma_load_3d_pair(a, mapL, bar, k0, row0, T.mat);
+          tma_load_3d_pair(a + kBox, mapL, bar, k0, row0 + 64, T.mat);
+        }
+        if (Kind<KIND>::r_mn) {
+          tma_load_3d_pair(b, mapR, bar, col0, k0, T.mat);
+          tma_load_3d_pair(b + kBox, mapR, bar, col0 + 64, k0, T.mat);
+        } else {
+          tma_load_3d_pair(b, mapR, bar, k0, col0, T.mat);
+          tma_load_3d_pair(b + kBox, mapR, bar, k0, col0 + 64, T.mat);
+        }
       }
       if (++stage == kStages) {
         stage = 0;
@@ -255,11 +266,12 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
   for (int t = int(cluster_id_x()); t < g.total_tiles; t += clusters, ++it) {
     if (cur.seek(g, g.tile_base + t)) KB = (k_extent<KIND>(g, g.buckets[cur.b]) + kBK - 1) / kBK;
     // Descriptors of stage 0, K-step 0; the start-address field (bits 0-13,
-    // address >> 4) then advances by a constant per stage and per K-step of
-    // 16 elements: K-major 32 bytes along the swizzled 128-byte row (8-row
-    // groups 1 KB apart); MN-major 2 KB = 16 K-rows (64-element atoms 8 KB
-    // apart, LBO; 8-row K groups 1 KB apart, SBO).  Shared-memory addresses
-    // stay below 256 KB, so the field never carries into the next one.
+    // address >> 4) then advances by a constant per stage, per 64-element
+    // panel and per K-step of 16 elements within a panel: K-major 32 bytes
+    // along the swizzled 128-byte row (8-row groups 1 KB apart); MN-major
+    // 2 KB = 16 K-rows (64-element atoms 8 KB apart, LBO; 8-row K groups 1 KB
+    // apart, SBO).  Shared-memory addresses stay below 256 KB, so the field
+    // never carries into the next one.
     const uint64_t a_desc = sdesc_sw128(a0, Kind<KIND>::l_mn ? kBox : 16, 1024);
     const uint64_t b_desc = sdesc_sw128(b0, Kind<KIND>::r_mn ? kBox : 16, 1024);
     constexpr uint32_t a_kstep = Kind<KIND>::l_mn ? (2048u >> 4) : (32u >> 4);
@@ -289,7 +301,9 @@ DM_DEV void mma_issuer(const GemmArgs& g, uint8_t* sA, uint8_t* sB, uint64_t* fu
       const uint64_t bd = b_desc + uint64_t(stage * (kBStage >> 4));
 #pragma unroll
       for (int k = 0; k < kBK / 16; ++k)
-        umma_bf16_pair(d, ad + k * a_kstep, bd + k * b_kstep, idesc, (kb | k) != 0 ? 1u : 0u);
+        umma_bf16_pair(d, ad + (k >> 2) * (kAPanel >> 4) + (k & 3) * a_kstep,
+                       bd + (k >> 2) * (kBPanel >> 4) + (k & 3) * b_kstep, idesc,
+                       (kb | k) != 0 ? 1u : 0u);
       umma_commit_pair(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
       if (++stage == kStages) {
         stage = 0;

@@ -104,8 +104,9 @@ struct InternalMat {
 enum ProductKind : int { kSymK = 0, kSymMN = 1, kFullWide = 2, kFullTall = 3 };
 
 // Tile shape of the Newton-Schulz products: a CTA pair computes a 256 x 256
-// tile; each CTA holds 128 of its rows (and loads half of its columns' operand).
-constexpr int kTileM = 256, kTileN = 256, kCtaM = 128, kBK = 64;
+// tile; each CTA holds 128 of its rows (and loads half of its columns'
+// operand); one pipeline stage carries kBK = 128 of the reduction dimension.
+constexpr int kTileM = 256, kTileN = 256, kCtaM = 128, kBK = 128;
 
 // One record per CTA of a traced product launch (see dmuon_trace_begin):
 // %globaltimer nanoseconds at kernel entry, at the leader's first MMA issue,
