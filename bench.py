@@ -16,6 +16,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -48,7 +49,10 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling during the timed region.  Each
+    sample keeps its host arrival time, so that a short timed region can be
+    summarised from its own samples only (`stop(window=(t0, t1))`, times from
+    time.monotonic()) rather than from idle ones around it."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -73,9 +77,9 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
-    def stop(self):
+    def stop(self, window=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -87,7 +91,9 @@ class ClockSampler:
             self.thread.join(timeout=5)
         sm, smax, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
+            if window is not None and not (window[0] <= t <= window[1]):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -327,11 +333,15 @@ OTHER_CONFIGS = [("single-256x1024", 0, 5), ("qwen2.5-1.5b", 0, 5), ("llama-3.2-
                  ("qwen2.5-7b", 1, 5), ("qwen2.5-7b", 0, 8), ("qwen2.5-7b", 1, 8)]
 
 
-def config_point(dmuon, wl, name, variant, ns_steps, dev, gpu_index, peak, steps=3, warmup=3):
+def config_point(dmuon, wl, name, variant, ns_steps, dev, gpu_index, peak, steps=3, warmup=3,
+                 min_region_s=0.5, max_steps=20):
     """One configuration, measured like the main workload but shorter: the whole
-    step through dmuon_muon_step (median of `steps`), then the same step as
-    three calls with events between them for the Newton-Schulz phase; per-owner
-    times where the set has an owner partition.  Clocks sampled throughout."""
+    step through dmuon_muon_step (median of the timed steps), then the same step
+    as three calls with events between them for the Newton-Schulz phase;
+    per-owner times where the set has an owner partition.  Short steps are
+    repeated (up to `max_steps`) until each of the two timed regions lasts
+    about `min_region_s`, and the clocks are summarised from the samples taken
+    inside them only."""
     import torch
     w = wl.WORKLOADS[name]
     shapes = w.shapes()
@@ -356,9 +366,15 @@ def config_point(dmuon, wl, name, variant, ns_steps, dev, gpu_index, peak, steps
     for _ in range(warmup):
         step()
     barrier()
+    t_one = time.perf_counter()
+    step()
+    barrier()
+    t_one = time.perf_counter() - t_one
+    steps = max(steps, min(max_steps, int(math.ceil(min_region_s / max(t_one, 1e-6)))))
     sampler = ClockSampler(gpu_index)
     sampler.start()
     time.sleep(0.3)
+    t_region0 = time.monotonic()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     ev[0].record(stream)
     for k in range(steps):
@@ -380,7 +396,7 @@ def config_point(dmuon, wl, name, variant, ns_steps, dev, gpu_index, peak, steps
                                 owner.workspace, stream=stream)
             ph[k][3].record(stream)
     barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(window=(t_region0, time.monotonic()))
     st = dmuon.stream_status(owner.workspace, stream)
     if st != dmuon.OK:
         raise RuntimeError(f"{name}: {dmuon.status_string(st)}")
@@ -534,6 +550,7 @@ def run_gpu(args, rank, world, local_rank):
     # timed region 1 -- `value`: the product call, dmuon_muon_step, once per step
     step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     barrier()
+    t_region0 = time.monotonic()
     dmuon.launch_count(reset=True)
     torch.cuda.nvtx.range_push("whole_step")   # for profiler selection (ncu --nvtx-include)
     step_ev[0].record(stream)
@@ -552,7 +569,7 @@ def run_gpu(args, rank, world, local_rank):
         step_phases(evs[k])
     torch.cuda.nvtx.range_pop()
     barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(window=(t_region0, time.monotonic()))
     st = dmuon.stream_status(owner.workspace, stream)
     if st != dmuon.OK:
         raise RuntimeError(f"timed steps failed: {dmuon.status_string(st)}")

@@ -120,3 +120,29 @@ def test_nominal_flops_count_every_product_in_full():
     m, n = 1024, 4096
     assert b.nominal_flops(s, 5) == pytest.approx(5 * (2 * m * m * n + 2 * m ** 3 + 2 * m * m * n))
     assert b.nominal_flops(s, 5) > b.ns_flops(s, 5)
+
+
+def test_clock_sampler_keeps_only_samples_inside_the_window():
+    """A short timed region is summarised from its own samples: idle samples
+    before and after it (maximum clock, low power) do not enter the median."""
+    class FakeProc:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    s = _bench().ClockSampler(0)
+    s.proc = FakeProc()
+    row = "0, {mhz}, 2070, {w}, 0x0, Not Active, Not Active, Not Active, {cap}"
+    s.lines = [(0.0, row.format(mhz=2070, w=200, cap="Not Active")),
+               (1.0, row.format(mhz=1500, w=1300, cap="Active")),
+               (1.2, row.format(mhz=1520, w=1350, cap="Active")),
+               (1.4, row.format(mhz=1480, w=1340, cap="Active")),
+               (3.0, row.format(mhz=2070, w=210, cap="Not Active"))]
+    inside = s.stop(window=(0.9, 1.5))
+    assert inside["samples"] == 3 and inside["sm_mhz"] == 1500
+    assert inside["power_w_median"] == 1340 and inside["reasons"] == ["sw_power_cap"]
+    s.proc = FakeProc()
+    everything = s.stop()
+    assert everything["samples"] == 5 and everything["sm_mhz"] == 1520
