@@ -334,7 +334,7 @@ OTHER_CONFIGS = [("single-256x1024", 0, 5), ("qwen2.5-1.5b", 0, 5), ("llama-3.2-
 
 
 def config_point(dmuon, wl, name, variant, ns_steps, dev, gpu_index, peak, steps=3, warmup=3,
-                 min_region_s=0.5, max_steps=20):
+                 min_region_s=0.5, max_steps=2000):
     """One configuration, measured like the main workload but shorter: the whole
     step through dmuon_muon_step (median of the timed steps), then the same step
     as three calls with events between them for the Newton-Schulz phase;
