@@ -233,7 +233,9 @@ int build_plan(int n, const dmuon_shape* shp, int variant, int ns_steps, Plan& P
   P.off_imat = off;
   off = align_up(off + size_t(P.n_internal) * sizeof(InternalMat), 16);
   P.off_sym = off;
-  off = align_up(off + size_t(P.sym_total) * sizeof(int), 128);
+  off = align_up(off + size_t(P.sym_total) * sizeof(int), 16);
+  // the TMA unit reads a tensor map only from a 64-byte aligned address
+  off = align_up(off, 128);
   P.off_tmaps = off;
   off = align_up(off + P.buckets.size() * kMapsPerBucket * 128, 16);
   P.tables_bytes = off - P.off_tables;
@@ -448,6 +450,8 @@ int upload_tables(const Request& R, const Plan& P) {
   InternalMat* im = reinterpret_cast<InternalMat*>(at(P.off_imat));
   int* sym = reinterpret_cast<int*>(at(P.off_sym));
   CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(at(P.off_tmaps));
+  // a tensor map the TMA unit cannot read faults the kernel: refuse instead
+  if ((reinterpret_cast<uintptr_t>(ws + P.off_tmaps) & 63u) != 0) return DMUON_ERR_ALIGNMENT;
 
   for (int i = 0; i < P.n; ++i) {
     EwMat& E = ew[P.ew_pos[i]];
