@@ -137,6 +137,39 @@ def test_ns_batched_odd_shapes(dm, wl, steps):
         assert err <= NS_TOL[steps], f"{s} steps={steps}: rel err {err:.3e}"
 
 
+# m and n on both sides of the product kernel's boundaries: a pipeline stage
+# carries 128 of the reduction dimension, a tile 256 rows and columns, a TMA box
+# 64; both orientations
+BOUNDARY_SHAPES = [(127, 384), (128, 385), (129, 383), (255, 511), (256, 513), (257, 640),
+                   (383, 129), (384, 128), (385, 127), (511, 255), (513, 256), (640, 257),
+                   (384, 384), (385, 385), (63, 129), (129, 63)]
+
+
+@pytest.mark.parametrize("steps,variant", [(1, 0), (5, 0), (5, 1)])
+def test_ns_stage_and_tile_boundaries(dm, wl, steps, variant):
+    """Shapes whose m and n fall just below, on and just above the multiples of
+    64, 128 and 256 that the product kernel's boxes, stages and tiles use, in
+    both orientations; with the Gram rule, the shapes it gives the Gram form are
+    checked against the oracle's Gram iteration."""
+    ps = PackedSet(dm, BOUNDARY_SHAPES, variant=variant)
+    ins = []
+    for i, s in enumerate(BOUNDARY_SHAPES):
+        u = wl.random_matrix(s, 900 + i, "cuda", 1.0, torch.bfloat16)
+        ps.view(i).copy_(u)
+        ins.append(np64(u))
+    run_ns(dm, ps, steps, variant=variant)
+    assert ps.guards_intact()
+    n_gram = 0
+    for i, s in enumerate(BOUNDARY_SHAPES):
+        gram = dm.ns_variant_for(s, steps, variant) == dm.NS_GRAM
+        n_gram += gram
+        ref = (oracle.gram_newton_schulz if gram else oracle.newton_schulz)(ins[i], steps)
+        err = rel(np64(ps.view(i)), ref)
+        assert err <= NS_TOL[steps], f"{s} steps={steps} gram={gram}: rel err {err:.3e}"
+    if variant == dm.NS_GRAM:
+        assert n_gram > 0
+
+
 @pytest.mark.parametrize("steps", [0, 1])
 def test_ns_eps_is_added_to_the_norm(dm, wl, steps):
     """With ||U|| ~ 1e-3 and eps = 1e-3, X0 = U / (||U|| + eps) is about half of
