@@ -89,6 +89,11 @@ WORKLOADS: Dict[str, Workload] = {
     # the device with workspace): the same kernels on a case small enough for
     # multi-pass profiler captures.
     "llama-3.1-8b-layer": Workload("llama-3.1-8b-layer", 5, 1, _layer(4096, 1024, 14336)),
+    # One layer of the Qwen2.5-1.5B set with the model's (tied) embedding as its
+    # AdamW parameters (233 M elements, ~4 GB on the device in all): the AdamW
+    # kernel on a case small enough for multi-pass profiler captures.
+    "qwen2.5-1.5b-layer": Workload("qwen2.5-1.5b-layer", 6, 1, _layer(1536, 256, 8960),
+                                   vocab=151936, tied_head=True),
 }
 
 
