@@ -388,14 +388,17 @@ def test_muon_step_bf16_weights_ragged_buckets(dm, wl):
     _muon_case(dm, wl, shapes, torch.bfloat16, torch.bfloat16, seed=23)
 
 
-def test_nan_and_inf_propagate_to_their_own_matrix_only(dm, wl):
+@pytest.mark.parametrize("variant", [0, 1])
+def test_nan_and_inf_propagate_to_their_own_matrix_only(dm, wl, variant):
     """A NaN in one gradient and an Inf in another: those two matrices' O and
     W become NaN everywhere, exactly as in the oracle (X0 = U/||U|| is NaN at
     the bad element, and every product spreads it over the whole matrix); the
     momentum keeps the bad value at its element only; every other matrix of the
-    same call, in the same buckets, matches the oracle as usual."""
+    same call, in the same buckets, matches the oracle as usual.  With the Gram
+    rule the rectangular matrices take the Gram form, whose products spread the
+    bad value the same way."""
     shapes = [(256, 700), (256, 700), (256, 700), (700, 256), (700, 256), (300, 300)]
-    own = dm.MuonOwner(shapes)
+    own = dm.MuonOwner(shapes, variant=variant)
     ws = [wl.random_matrix(s, 1500 + i, "cuda", 0.02, torch.bfloat16) for i, s in enumerate(shapes)]
     ms = [torch.zeros(s, device="cuda") for s in shapes]
     gs = [wl.random_matrix(s, 1600 + i, "cuda", 1e-3, torch.bfloat16) for i, s in enumerate(shapes)]
@@ -404,9 +407,13 @@ def test_nan_and_inf_propagate_to_their_own_matrix_only(dm, wl):
     w0 = [np64(w) for w in ws]
     own.step(gs, ms, ws, lr=0.02, beta=0.95, ns_steps=5)
     assert own.status() == dm.OK
+    n_gram = 0
     for i, s in enumerate(shapes):
+        gram = dm.ns_variant_for(s, 5, variant) == dm.NS_GRAM
+        n_gram += gram
         m_ref, o_ref, w_ref = oracle.muon_step(np64(gs[i]), np.zeros(s), w0[i], lr=0.02,
-                                               beta=0.95, ns_steps=5)
+                                               beta=0.95, ns_steps=5,
+                                               variant="gram" if gram else "standard")
         m_gpu, o_gpu, w_gpu = np64(ms[i]), np64(own.packed_view(i)), np64(ws[i])
         if i in (1, 3):
             assert np.isnan(o_ref).all() and np.isnan(w_ref).all()
@@ -421,6 +428,7 @@ def test_nan_and_inf_propagate_to_their_own_matrix_only(dm, wl):
             assert np.isfinite(o_gpu).all() and np.isfinite(w_gpu).all(), f"#{i} touched"
             assert rel(m_gpu, m_ref) <= 1e-5
             assert rel(o_gpu, o_ref) <= NS_TOL[5], f"#{i}: O rel err {rel(o_gpu, o_ref):.3e}"
+    assert n_gram == (5 if variant == 1 else 0)
 
 
 def test_two_owners_on_two_streams_run_concurrently_and_match(dm, wl):
