@@ -33,6 +33,8 @@ EXPORTED = ("dmuon_plan", "dmuon_workspace_bytes", "dmuon_ns_variant_for", "dmuo
             "dmuon_adamw_workspace_bytes", "dmuon_status_string", "dmuon_version",
             "dmuon_launch_count", "dmuon_trace_begin", "dmuon_trace_end")
 NOALLOC_SCRATCH_BYTES = 64 << 20
+# largest short side m and long side n of a matrix the library accepts
+MAX_M, MAX_N = 32768, 1048576
 
 
 class Shape(ctypes.Structure):

@@ -175,3 +175,16 @@ def test_ns_variant_rule_properties(dm):
         dm.ns_variant_for((4, 8), -1, dm.NS_GRAM)
     with pytest.raises(dm.DMuonError):
         dm.ns_variant_for((4, 8), 5, 7)
+
+
+def test_binding_size_limits_match_the_header(dm):
+    """The binding's MAX_M / MAX_N mirror DMUON_MAX_M / DMUON_MAX_N, and the
+    library accepts a matrix exactly at both limits and refuses one beyond."""
+    text = open(os.path.join(ROOT, "include", "dmuon.h")).read()
+    assert int(re.search(r"#define DMUON_MAX_M (\d+)", text).group(1)) == dm.MAX_M
+    assert int(re.search(r"#define DMUON_MAX_N (\d+)", text).group(1)) == dm.MAX_N
+    assert dm.workspace_bytes([(dm.MAX_M, dm.MAX_M)], 0) > 0
+    assert dm.workspace_bytes([(64, dm.MAX_N)], 0) > 0
+    assert dm.workspace_bytes([(dm.MAX_N, 64)], 0) > 0
+    assert dm.workspace_bytes([(64, dm.MAX_N + 1)], 0) == 0
+    assert dm.workspace_bytes([(dm.MAX_M + 1, dm.MAX_M + 1)], 0) == 0
