@@ -196,8 +196,9 @@ int dmuon_unpack_update(int n, const dmuon_shape* shp, void* const* weight,
  * and while one group is orthogonalised, later groups are packed and relaid
  * out and earlier groups' weights are updated, in pieces that each start
  * together with one long product launch and are sized to finish inside it;
- * what does not fit -- the packs of the first groups, the last group's update
- * -- runs alone on `stream`.  The overlapped work runs on a
+ * what does not fit -- the first group's pack, the part of a later group's
+ * pack that the products before it cannot hide (run just before that group),
+ * the last group's update -- runs alone on `stream`.  The overlapped work runs on a
  * lowest-priority companion stream that the library creates for `stream` on
  * its first call with it (one per caller stream, up to 16 per device; past
  * that, and while `stream` is being captured, a companion shared by the device

@@ -733,7 +733,8 @@ struct Piece {
 
 struct StepSchedule {
   std::vector<std::pair<int, int>> pos;               // bucket range [b0, b1) of each position
-  std::vector<char> prepacked;                        // per position: packed on `s` first
+  std::vector<std::vector<Piece>> pre;               // per position: its pack work left for `s`,
+                                                      // right before its products
   std::vector<std::vector<std::vector<Piece>>> slot;  // [position][launch]: pieces next to it
   std::vector<Piece> tail_update;                     // update ranges run on `s` at the end
   double products = 0.0, exposed = 0.0;               // modelled seconds
@@ -791,17 +792,16 @@ PieceCosts piece_costs(const Request& R) {
 // Greedy placement for one sequence of positions.  Slots are the product
 // phases in issue order; each takes, up to its budget, first the pack/relayout
 // work of the nearest later position (needed before that position's products
-// start), then the updates of earlier positions.  A position whose pack cannot
-// be finished in the slots before its products is packed on `s` up front
-// instead, and the placement is redone.
+// start), then the updates of earlier positions.  The part of a position's pack
+// that the slots before it cannot take (all of it for the first position) runs
+// on `s` just before its products, after the part that did run beside them.
 StepSchedule plan_step(const Plan& P, const Request& R,
                        const std::vector<std::pair<int, int>>& pos, int clusters) {
   const int g = int(pos.size());
   const PieceCosts pc = piece_costs(R);
   StepSchedule S;
   S.pos = pos;
-  S.prepacked.assign(size_t(g), 0);
-  S.prepacked[0] = 1;
+  S.pre.assign(size_t(g), {});
   std::vector<std::vector<double>> dur(static_cast<size_t>(g));
   S.products = 0.0;
   for (int k = 0; k < g; ++k) {
@@ -813,70 +813,62 @@ StepSchedule plan_step(const Plan& P, const Request& R,
       S.products += dur[size_t(k)].back();
     }
   }
-  for (;;) {
-    S.slot.assign(size_t(g), std::vector<std::vector<Piece>>());
-    for (int k = 0; k < g; ++k) S.slot[size_t(k)].assign(dur[size_t(k)].size(), {});
-    S.tail_update.clear();
-    struct Todo { int pos, kind, bucket; long long lo, hi; };
-    std::vector<Todo> mb, upd;
-    for (int k = 0; k < g; ++k)
-      for (int b = pos[size_t(k)].first; b < pos[size_t(k)].second; ++b) {
-        const long long ch = P.buckets[b].chunks;
-        if (!S.prepacked[size_t(k)]) {
-          mb.push_back({k, kPiecePack, b, 0, ch});
-          mb.push_back({k, kPieceFinalize, b, 0, 1});
-          mb.push_back({k, kPieceRelayout, b, 0, ch});
-        }
-        upd.push_back({k, kPieceUpdate, b, 0, ch});
-      }
-    size_t mi = 0, ui = 0;
-    int fail = -1;
-    for (int k = 0; k < g && fail < 0; ++k) {
-      // every later position's pack must be done before its products start
-      if (mi < mb.size() && mb[mi].pos <= k) fail = mb[mi].pos;
-      for (size_t i = 0; i < dur[size_t(k)].size() && fail < 0; ++i) {
-        double budget = dur[size_t(k)][i] * kModelCoBytes * kSlotFill;
-        if (budget < kMinPieceBytes) continue;
-        std::vector<Piece>& out = S.slot[size_t(k)][i];
-        auto take = [&](Todo& t, double unit_bytes) {
-          const long long can = unit_bytes > 0 ? (long long)(budget / unit_bytes) : t.hi - t.lo;
-          const long long n = std::min(can, t.hi - t.lo);
-          if (n <= 0) return false;
-          out.push_back({t.kind, t.bucket, t.lo, t.lo + n});
-          budget -= double(n) * unit_bytes;
-          t.lo += n;
-          return t.lo == t.hi;
-        };
-        while (mi < mb.size()) {
-          Todo& t = mb[mi];
-          const double ub = t.kind == kPiecePack ? pc.pack_chunk
-                            : t.kind == kPieceRelayout ? pc.relay_chunk : 0.0;
-          if (!take(t, ub)) break;
-          ++mi;
-        }
-        while (ui < upd.size() && upd[ui].pos < k) {
-          if (!take(upd[ui], pc.update_chunk)) break;
-          ++ui;
-        }
-      }
-    }
-    if (fail < 0 && mi < mb.size()) fail = mb[mi].pos;
-    if (fail >= 0) {  // pack that position up front and place again
-      S.prepacked[size_t(fail)] = 1;
-      continue;
-    }
-    // updates left over (the unplaced rest of each) run on `s` after the last products
-    for (; ui < upd.size(); ++ui)
-      if (upd[ui].lo < upd[ui].hi)
-        S.tail_update.push_back({kPieceUpdate, upd[ui].bucket, upd[ui].lo, upd[ui].hi});
-    break;
-  }
-  S.exposed = 0.0;
+  S.slot.assign(size_t(g), std::vector<std::vector<Piece>>());
+  for (int k = 0; k < g; ++k) S.slot[size_t(k)].assign(dur[size_t(k)].size(), {});
+  struct Todo { int pos, kind, bucket; long long lo, hi; };
+  std::vector<Todo> mb, upd;
   for (int k = 0; k < g; ++k)
-    if (S.prepacked[size_t(k)])
-      for (int b = pos[size_t(k)].first; b < pos[size_t(k)].second; ++b)
-        S.exposed += double(P.buckets[b].chunks) * (pc.pack_chunk + pc.relay_chunk) /
-                     kModelHbmBytes;
+    for (int b = pos[size_t(k)].first; b < pos[size_t(k)].second; ++b) {
+      const long long ch = P.buckets[b].chunks;
+      mb.push_back({k, kPiecePack, b, 0, ch});
+      mb.push_back({k, kPieceFinalize, b, 0, 1});
+      mb.push_back({k, kPieceRelayout, b, 0, ch});
+      upd.push_back({k, kPieceUpdate, b, 0, ch});
+    }
+  size_t mi = 0, ui = 0;
+  for (int k = 0; k < g; ++k) {
+    // a position's pack must be done before its products start: what the
+    // earlier slots could not take runs on `s` just before them
+    for (; mi < mb.size() && mb[mi].pos <= k; ++mi)
+      if (mb[mi].lo < mb[mi].hi)
+        S.pre[size_t(k)].push_back({mb[mi].kind, mb[mi].bucket, mb[mi].lo, mb[mi].hi});
+    for (size_t i = 0; i < dur[size_t(k)].size(); ++i) {
+      double budget = dur[size_t(k)][i] * kModelCoBytes * kSlotFill;
+      if (budget < kMinPieceBytes) continue;
+      std::vector<Piece>& out = S.slot[size_t(k)][i];
+      auto take = [&](Todo& t, double unit_bytes) {
+        const long long can = unit_bytes > 0 ? (long long)(budget / unit_bytes) : t.hi - t.lo;
+        const long long n = std::min(can, t.hi - t.lo);
+        if (n <= 0) return false;
+        out.push_back({t.kind, t.bucket, t.lo, t.lo + n});
+        budget -= double(n) * unit_bytes;
+        t.lo += n;
+        return t.lo == t.hi;
+      };
+      while (mi < mb.size()) {
+        Todo& t = mb[mi];
+        const double ub = t.kind == kPiecePack ? pc.pack_chunk
+                          : t.kind == kPieceRelayout ? pc.relay_chunk : 0.0;
+        if (!take(t, ub)) break;
+        ++mi;
+      }
+      while (ui < upd.size() && upd[ui].pos < k) {
+        if (!take(upd[ui], pc.update_chunk)) break;
+        ++ui;
+      }
+    }
+  }
+  // updates left over (the unplaced rest of each) run on `s` after the last products
+  S.tail_update.clear();
+  for (; ui < upd.size(); ++ui)
+    if (upd[ui].lo < upd[ui].hi)
+      S.tail_update.push_back({kPieceUpdate, upd[ui].bucket, upd[ui].lo, upd[ui].hi});
+  S.exposed = 0.0;
+  for (const auto& v : S.pre)
+    for (const Piece& t : v)
+      S.exposed += double(t.hi - t.lo) *
+                   (t.kind == kPiecePack ? pc.pack_chunk
+                    : t.kind == kPieceRelayout ? pc.relay_chunk : 0.0) / kModelHbmBytes;
   for (const Piece& t : S.tail_update)
     S.exposed += double(t.hi - t.lo) * pc.update_chunk / kModelHbmBytes;
   return S;
@@ -1041,46 +1033,45 @@ int run(const Request& R) {
     std::vector<int> pos_of(static_cast<size_t>(nb), 0);
     for (int k = 0; k < g; ++k)
       for (int b = S.pos[size_t(k)].first; b < S.pos[size_t(k)].second; ++b) pos_of[size_t(b)] = k;
-    // packs up front, on `s`, at full speed
-    for (int k = 0; k < g; ++k) {
-      if (!S.prepacked[size_t(k)]) continue;
-      const EwRange r = range_of(S.pos[size_t(k)].first, S.pos[size_t(k)].second);
-      if (launch_momentum_pack(r, gbf16, R.beta, packed, partials, s) != cudaSuccess ||
-          launch_norm_finalize(r, partials, R.eps, inv, s) != cudaSuccess ||
-          launch_relayout(r, packed, inv, s) != cudaSuccess)
-        return DMUON_ERR_CUDA;
-    }
-    // one piece on the aux stream
-    auto run_piece = [&](const Piece& pc) {
+    // one piece of memory-bound work on stream `st`; pack work of a position
+    // that runs on the aux stream records the position's event after it, so
+    // that the caller's stream can wait for all of it before the position's
+    // products (the last record before that wait is the one that counts)
+    std::vector<char> aux_pack(static_cast<size_t>(g), 0);
+    auto run_piece = [&](const Piece& pc, cudaStream_t st) {
       EwRange r = bucket_range(pc.bucket);
+      bool ok = true;
       switch (pc.kind) {
         case kPiecePack:
           r.chunk_base += pc.lo;
           r.chunks = pc.hi - pc.lo;
-          return launch_momentum_pack(r, gbf16, R.beta, packed, partials, x) == cudaSuccess;
+          ok = launch_momentum_pack(r, gbf16, R.beta, packed, partials, st) == cudaSuccess;
+          break;
         case kPieceFinalize:
-          return launch_norm_finalize(r, partials, R.eps, inv, x) == cudaSuccess;
-        case kPieceRelayout: {
+          ok = launch_norm_finalize(r, partials, R.eps, inv, st) == cudaSuccess;
+          break;
+        case kPieceRelayout:
           r.chunk_base += pc.lo;
           r.chunks = pc.hi - pc.lo;
-          if (launch_relayout(r, packed, inv, x) != cudaSuccess) return false;
-          // the position is ready for its products after the last relayout piece
-          // of its last bucket
-          const int k = pos_of[size_t(pc.bucket)];
-          if (pc.hi == P.buckets[pc.bucket].chunks && pc.bucket + 1 == S.pos[size_t(k)].second &&
-              cudaEventRecord(ev.e[size_t(k)], x) != cudaSuccess)
-            return false;
-          return true;
-        }
+          ok = launch_relayout(r, packed, inv, st) == cudaSuccess;
+          break;
         default:
           r.chunk_base += pc.lo;
           r.chunks = pc.hi - pc.lo;
-          return launch_update(r, wbf16, R.lr, packed, x) == cudaSuccess;
+          return launch_update(r, wbf16, R.lr, packed, st) == cudaSuccess;
       }
+      if (ok && st == x) {
+        const int k = pos_of[size_t(pc.bucket)];
+        aux_pack[size_t(k)] = 1;
+        ok = cudaEventRecord(ev.e[size_t(k)], x) == cudaSuccess;
+      }
+      return ok;
     };
     for (int k = 0; k < g; ++k) {
-      if (!S.prepacked[size_t(k)] && cudaStreamWaitEvent(s, ev.e[size_t(k)], 0) != cudaSuccess)
+      if (aux_pack[size_t(k)] && cudaStreamWaitEvent(s, ev.e[size_t(k)], 0) != cudaSuccess)
         return DMUON_ERR_CUDA;
+      for (const Piece& pc : S.pre[size_t(k)])
+        if (!run_piece(pc, s)) return DMUON_ERR_CUDA;
       auto before = [&](int i) {
         const auto& pieces = S.slot[size_t(k)][size_t(i)];
         if (pieces.empty()) return true;
@@ -1089,7 +1080,7 @@ int run(const Request& R) {
         if (cudaEventRecord(e, s) != cudaSuccess || cudaStreamWaitEvent(x, e, 0) != cudaSuccess)
           return false;
         for (const Piece& pc : pieces)
-          if (!run_piece(pc)) return false;
+          if (!run_piece(pc, x)) return false;
         return true;
       };
       const GemmLauncher L(P, R, D.max_clusters, ws, S.pos[size_t(k)].first,
